@@ -1,0 +1,18 @@
+"""CPU oracle of the fine-grained FP8 block-scaled linear layer.
+
+Test infrastructure only: imported by the tests, the smoke check and the
+benchmark's CPU baseline leg, never by the product path.
+"""
+from .fp8_oracle import (  # noqa: F401
+    E4M3_MAX,
+    GROUP,
+    blockscaled_gemm,
+    blockscaled_grouped_gemm,
+    dequant_weight_128x128,
+    e4m3_decode,
+    e4m3_encode_rne_satfinite,
+    fl32_div,
+    linear_forward,
+    quant_act_1x128,
+    quant_weight_128x128,
+)

@@ -1,0 +1,238 @@
+"""Plain CPU oracle for the fine-grained FP8 block-scaled linear layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only the tests, the smoke check and the benchmark's CPU
+baseline leg use it.  It shares no code, table or constant generator with the
+CUDA library; it is a slow, direct restatement of the method so that a reader
+can check it against the source text by eye.
+
+Source: the DeepSeek-V3 FP8 mixed-precision framework excerpt reposted as
+"The Definitive Information To Deepseek":
+  * paragraph 3, "Figure 7 (a)" items (1) and (2): activations are grouped and
+    scaled on 1x128 tiles (per token per 128 channels), weights on 128x128
+    blocks (per 128 input channels per 128 output channels);
+  * paragraph 2, last sentence: a scaling factor is derived per group and the
+    activation or weight is quantised online into FP8;
+  * paragraph 4, first sentence: the GEMMs take FP8 tensors and produce BF16
+    (or FP32) outputs;
+  * paragraph 1, last sentence: partial sums are promoted (moved to a higher
+    precision accumulator) while the next MMA runs.
+
+Where the excerpt is silent the plainest reading is taken:
+  * the FP8 format is OCP E4M3FN (bias 7, largest finite 448, no infinities);
+  * the per-group statistic is the maximum absolute value (amax) and the FP32
+    scale is s = fl32(amax / 448); values are quantised as E4M3(fl32(x / s))
+    with round-to-nearest-even and saturation to +-448 (never NaN);
+  * an all-zero group has s = 0 and every code +0 (0x00);
+  * a value of a non-zero group that rounds to zero keeps its sign (0x80);
+  * promotion happens once per 128-wide K chunk, i.e. exactly at the scale
+    group boundaries, so
+        Y[m, n] = sum_kb  sa[kb, m] * sw[n // 128, kb]
+                          * sum_{k in chunk kb} dec(qa[m, k]) * dec(qw[n, k]);
+  * scales are laid out sa[kb, m] (token index contiguous) and
+    sw[nb, kb] (row-major over weight blocks).
+
+Precision: E4M3 products have at most 8 significant bits and lie in
+[2**-18, 448**2]; a sum of 128 of them fits in 43 bits, so every chunk sum
+below is exact in float64 whatever order the BLAS routine adds in.  The
+scales are float32, so sa * sw is exact in float64 too; only the final sum
+over K chunks rounds (at float64 precision).
+
+Rounded float32 division fl32(a / b) is computed as float32(float64(a) /
+float64(b)).  Rounding a quotient first to 53 and then to 24 bits gives the
+correctly rounded 24-bit quotient because 53 >= 2 * 24 + 2 (S. A. Figueroa,
+"When is double rounding innocuous?", SIGNUM Newsletter 30(3), 1995); the
+tests pin this against exact rational arithmetic.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0  # largest finite E4M3FN magnitude, code S.1111.110
+GROUP = 128       # group width along K (and block height along N for weights)
+
+
+# ---------------------------------------------------------------------------
+# E4M3FN codec, written from the format definition.
+# ---------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Exact float64 value of each OCP E4M3FN byte.
+
+    Layout S.EEEE.MMM with exponent bias 7:
+      E > 0 : (-1)**S * 2**(E - 7) * (1 + M / 8)
+      E = 0 : (-1)**S * 2**(-6)    * (M / 8)       (subnormals and +-0)
+      E = 15, M = 7 : NaN (the only non-finite codes, 0x7F and 0xFF).
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = c >> 7
+    exp = (c >> 3) & 0xF
+    man = c & 0x7
+    normal = np.ldexp(1.0 + man / 8.0, exp - 7)
+    subnormal = np.ldexp(man / 8.0, -6)
+    mag = np.where(exp == 0, subnormal, normal)
+    mag = np.where((exp == 15) & (man == 7), np.nan, mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+# Non-negative finite codes 0x00 .. 0x7E.  Their values increase with the
+# code, so consecutive codes are neighbouring representable values.
+_POS_CODES = np.arange(0x7F, dtype=np.int64)
+_POS_VALUES = e4m3_decode(_POS_CODES.astype(np.uint8))
+
+
+def e4m3_encode_rne_satfinite(v) -> np.ndarray:
+    """E4M3FN code of each float32 value: nearest representable value, ties to
+    the even code (mantissa LSB 0), magnitudes above 448 saturate to 448.
+
+    The sign is the sign bit of the input, so -0.0 and negative values that
+    round to zero both give 0x80.  NaN inputs are outside the contract.
+    """
+    v = np.asarray(v, dtype=np.float32)
+    a = np.abs(v).astype(np.float64)
+    # hi is the first non-negative code whose value is >= a.
+    hi = np.searchsorted(_POS_VALUES, a, side="left")
+    saturate = hi >= len(_POS_VALUES)  # a > 448
+    hi = np.minimum(hi, len(_POS_VALUES) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _POS_VALUES[hi] - a  # exact: both operands are short dyadic numbers
+    d_lo = a - _POS_VALUES[lo]
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (_POS_CODES[hi] % 2 == 0))
+    code = np.where(take_hi, hi, lo)
+    code = np.where(saturate, 0x7E, code)
+    code = code | (np.signbit(v).astype(np.int64) << 7)
+    return code.astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# Rounded float32 arithmetic.
+# ---------------------------------------------------------------------------
+
+def fl32_div(a, b) -> np.ndarray:
+    """Correctly rounded float32 quotient a / b of float32 operands (see the
+    module docstring for why the float64 detour is exact).  b == 0 gives a
+    non-finite result that callers never use."""
+    a64 = np.asarray(a, dtype=np.float32).astype(np.float64)
+    b64 = np.asarray(b, dtype=np.float32).astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return (a64 / b64).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Group quantisation ("Figure 7 (a)" grouping + online scaling).
+# ---------------------------------------------------------------------------
+
+def _quantise_groups(g: np.ndarray):
+    """Quantise every group along the last axis of ``g`` (float32).
+
+    Returns (codes uint8 with the shape of g, scales float32 with g.shape[:-1]).
+    """
+    amax = np.max(np.abs(g), axis=-1)            # exact in float32
+    s = fl32_div(amax, np.float32(E4M3_MAX))     # s = fl32(amax / 448)
+    v = fl32_div(g, s[..., None])                # fl32(x / s)
+    codes = e4m3_encode_rne_satfinite(v)
+    codes[s == 0] = 0                            # all-zero group: every code +0
+    return codes, s
+
+
+def quant_act_1x128(x):
+    """1x128 activation quantisation (one scale per token per 128 channels).
+
+    x  : float32 [M, K] holding BF16 values, K % 128 == 0.
+    Returns qa uint8 [M, K] (E4M3FN codes) and sa float32 [K/128, M]
+    (sa[kb, m] is the scale of row m, channels 128*kb .. 128*kb + 127).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    M, K = x.shape
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 128")
+    codes, s = _quantise_groups(x.reshape(M, K // GROUP, GROUP))
+    return codes.reshape(M, K), np.ascontiguousarray(s.T)
+
+
+def quant_weight_128x128(w):
+    """128x128 weight quantisation (one scale per 128 output x 128 input
+    channels).
+
+    w  : float32 [N, K] holding BF16 values (row n = output channel n),
+         N % 128 == 0, K % 128 == 0.
+    Returns qw uint8 [N, K] and sw float32 [N/128, K/128]
+    (sw[nb, kb] covers rows 128*nb.. and columns 128*kb..).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    if N % GROUP or K % GROUP:
+        raise ValueError("N and K must be multiples of 128")
+    NB, KB = N // GROUP, K // GROUP
+    # [NB, 128, KB, 128] -> [NB, KB, 128*128]: one row per block.
+    blocks = w.reshape(NB, GROUP, KB, GROUP).transpose(0, 2, 1, 3).reshape(NB, KB, GROUP * GROUP)
+    codes, s = _quantise_groups(blocks)
+    qw = codes.reshape(NB, KB, GROUP, GROUP).transpose(0, 2, 1, 3).reshape(N, K)
+    return np.ascontiguousarray(qw), s
+
+
+def dequant_weight_128x128(qw, sw):
+    """float64 W ~= dec(qw) * sw broadcast over each 128x128 block."""
+    qw = np.asarray(qw, dtype=np.uint8)
+    N, K = qw.shape
+    scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float64), GROUP, axis=0), GROUP, axis=1)
+    return e4m3_decode(qw) * scale
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled GEMM with per-128-K-chunk promotion.
+# ---------------------------------------------------------------------------
+
+def blockscaled_gemm(qa, sa, qw, sw):
+    """Y[m, n] = sum_kb sa[kb, m] * sw[n//128, kb] * (chunk kb of dec(qa) . dec(qw)^T).
+
+    qa uint8 [M, K], sa float32 [K/128, M], qw uint8 [N, K], sw float32
+    [N/128, K/128].  Returns float64 [M, N], unrounded (the GPU writes BF16).
+    """
+    qa = np.asarray(qa, dtype=np.uint8)
+    qw = np.asarray(qw, dtype=np.uint8)
+    sa = np.asarray(sa, dtype=np.float32)
+    sw = np.asarray(sw, dtype=np.float32)
+    M, K = qa.shape
+    N = qw.shape[0]
+    KB = K // GROUP
+    y = np.zeros((M, N), dtype=np.float64)
+    for kb in range(KB):
+        cols = slice(kb * GROUP, (kb + 1) * GROUP)
+        a = e4m3_decode(qa[:, cols])
+        b = e4m3_decode(qw[:, cols])
+        chunk = a @ b.T                                           # exact
+        row_scale = sa[kb, :M].astype(np.float64)                 # [M]
+        col_scale = np.repeat(sw[:, kb].astype(np.float64), GROUP)  # [N]
+        y += chunk * (row_scale[:, None] * col_scale[None, :])    # promotion
+    return y
+
+
+def blockscaled_grouped_gemm(offsets, qa, sa, qw, sw):
+    """Grouped (per-expert) block-scaled GEMM.
+
+    Rows offsets[g] .. offsets[g+1]-1 of qa / sa / Y belong to group g and are
+    multiplied by weight group g.  qw uint8 [G, N, K], sw float32
+    [G, N/128, K/128], offsets int [G+1] with offsets[0] == 0, non-decreasing.
+    Returns float64 [offsets[G], N].
+    """
+    offsets = [int(o) for o in offsets]
+    qa = np.asarray(qa, dtype=np.uint8)
+    sa = np.asarray(sa, dtype=np.float32)
+    G = len(offsets) - 1
+    N = qw.shape[1]
+    y = np.zeros((offsets[-1], N), dtype=np.float64)
+    for g in range(G):
+        r0, r1 = offsets[g], offsets[g + 1]
+        if r1 > r0:
+            y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])
+    return y
+
+
+def linear_forward(x, w):
+    """The whole hot path on float32 inputs holding BF16 values: quantise X
+    per 1x128 tile and W per 128x128 block, then the block-scaled GEMM."""
+    qa, sa = quant_act_1x128(x)
+    qw, sw = quant_weight_128x128(w)
+    return blockscaled_gemm(qa, sa, qw, sw), (qa, sa, qw, sw)

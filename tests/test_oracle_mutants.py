@@ -1,0 +1,100 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Every mutant is a one-line textual change to the oracle source, executed as
+a throw-away module on the CPU; the real oracle is never modified.  This
+shows the pins in oracle_pins.py are strong enough to catch a dropped term,
+a wrong sign, index or rounding rule, or a transposed operand.
+"""
+import os
+import types
+
+import pytest
+
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "fp8_oracle.py")
+
+MUTANTS = {
+    "ties_away_from_zero": (
+        "take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (_POS_CODES[hi] % 2 == 0))",
+        "take_hi = (d_hi < d_lo) | (d_hi == d_lo)"),
+    "ties_toward_zero": (
+        "take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (_POS_CODES[hi] % 2 == 0))",
+        "take_hi = (d_hi < d_lo)"),
+    "no_saturation": (
+        "code = np.where(saturate, 0x7E, code)",
+        "code = np.where(saturate, 0x7F, code)"),
+    "sign_of_zero_dropped": (
+        "code = code | (np.signbit(v).astype(np.int64) << 7)",
+        "code = code | ((v < 0).astype(np.int64) << 7)"),
+    "scale_by_reciprocal": (
+        "s = fl32_div(amax, np.float32(E4M3_MAX))",
+        "s = (amax * np.float32(1.0 / 448.0)).astype(np.float32)"),
+    "quantise_by_multiply": (
+        "v = fl32_div(g, s[..., None])",
+        "v = (g * fl32_div(np.float32(1.0), s)[..., None]).astype(np.float32)"),
+    "zero_group_not_cleared": (
+        "codes[s == 0] = 0",
+        "pass"),
+    "amax_without_abs": (
+        "amax = np.max(np.abs(g), axis=-1)",
+        "amax = np.max(g, axis=-1)"),
+    "decode_bias_8": (
+        "normal = np.ldexp(1.0 + man / 8.0, exp - 7)",
+        "normal = np.ldexp(1.0 + man / 8.0, exp - 8)"),
+    "decode_subnormal_exponent": (
+        "subnormal = np.ldexp(man / 8.0, -6)",
+        "subnormal = np.ldexp(man / 8.0, -7)"),
+    "weight_blocks_not_transposed": (
+        "blocks = w.reshape(NB, GROUP, KB, GROUP).transpose(0, 2, 1, 3).reshape(NB, KB, GROUP * GROUP)",
+        "blocks = w.reshape(NB, KB, GROUP * GROUP)"),
+    "act_scales_not_transposed": (
+        "return codes.reshape(M, K), np.ascontiguousarray(s.T)",
+        "return codes.reshape(M, K), np.ascontiguousarray(s.T[::-1])"),
+    "weight_scale_of_chunk_0": (
+        "col_scale = np.repeat(sw[:, kb].astype(np.float64), GROUP)",
+        "col_scale = np.repeat(sw[:, 0].astype(np.float64), GROUP)"),
+    "act_scale_of_chunk_0": (
+        "row_scale = sa[kb, :M].astype(np.float64)",
+        "row_scale = sa[0, :M].astype(np.float64)"),
+    "act_scale_dropped": (
+        "y += chunk * (row_scale[:, None] * col_scale[None, :])",
+        "y += chunk * (col_scale[None, :] + 0 * row_scale[:, None])"),
+    "weight_scale_rows_swapped": (
+        "col_scale = np.repeat(sw[:, kb].astype(np.float64), GROUP)",
+        "col_scale = np.repeat(sw[::-1, kb].astype(np.float64), GROUP)"),
+    "operand_columns_reversed": (
+        "chunk = a @ b.T",
+        "chunk = (a @ b.T)[:, ::-1]"),
+    "negated_product": (
+        "chunk = a @ b.T",
+        "chunk = -(a @ b.T)"),
+    "grouped_wrong_weight_scales": (
+        "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])",
+        "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[0])"),
+    "grouped_wrong_rows_for_scales": (
+        "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])",
+        "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, :r1 - r0], qw[g], sw[g])"),
+}
+
+
+def _mutant_module(old, new):
+    with open(SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site not found exactly once: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    mod.__file__ = SRC
+    exec(compile(src.replace(old, new), SRC + " (mutant)", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    old, new = MUTANTS[name]
+    mod = _mutant_module(old, new)
+    for pin in ALL_PINS:
+        try:
+            pin(mod)
+        except Exception:
+            return  # caught
+    pytest.fail(f"mutant {name} passed every pin")
