@@ -1,0 +1,29 @@
+"""Fine-grained FP8 block-scaled linear layer for B300 (sm_103a).
+
+The compute path is the C-ABI library libfp8bs.so (include/fp8bs.h); the
+names below are its thin ctypes binding, loaded on first use.  `workloads`
+(seeded synthetic inputs) needs no GPU and no library.
+"""
+import importlib
+
+from . import workloads  # noqa: F401
+
+_API = (
+    "fp8_quant_act_1x128",
+    "fp8_quant_weight_128x128",
+    "fp8_blockscaled_gemm",
+    "fp8_blockscaled_grouped_gemm",
+    "fp8bs_last_device_error",
+    "fp8bs_set_wait_timeout_ns",
+    "fp8bs_selftest_wait_timeout",
+    "linear_forward",
+    "ld_sa_for",
+    "Fp8bsError",
+)
+
+
+def __getattr__(name):
+    if name in _API or name == "binding":
+        binding = importlib.import_module(__name__ + ".binding")
+        return binding if name == "binding" else getattr(binding, name)
+    raise AttributeError(name)

@@ -1,0 +1,186 @@
+"""ctypes binding of libfp8bs.so (declared in include/fp8bs.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (torch provides device memory
+and the current stream); outputs are allocated here when not supplied.
+There is no CPU fallback: importing this module fails loudly when the
+library has not been built, and every call fails on a host without a GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m fp8_fine_grained_14_b300.build` "
+        "(or __graft_entry__.build()); there is no fallback implementation")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_i64, _i32, _u64, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64, ctypes.c_void_p
+
+STATUS = {0: "FP8BS_OK", 1: "FP8BS_ERR_INVALID_ARG", 2: "FP8BS_ERR_MISALIGNED",
+          3: "FP8BS_ERR_UNSUPPORTED_SHAPE", 4: "FP8BS_ERR_CUDA", 5: "FP8BS_ERR_TIMEOUT"}
+EXPORTS = {
+    "fp8_quant_act_1x128": [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
+    "fp8_quant_weight_128x128": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
+    "fp8_blockscaled_gemm": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
+    "fp8_blockscaled_grouped_gemm": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
+    "fp8bs_status_string": [ctypes.c_int],
+    "fp8bs_last_error_detail": [],
+    "fp8bs_last_device_error": [_p],
+    "fp8bs_set_wait_timeout_ns": [_u64],
+    "fp8bs_selftest_wait_timeout": [_u64, _p],
+}
+for _name, _args in EXPORTS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = ctypes.c_int
+lib.fp8bs_status_string.restype = ctypes.c_char_p
+lib.fp8bs_last_error_detail.restype = ctypes.c_char_p
+lib.fp8bs_set_wait_timeout_ns.restype = None
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = lib.fp8bs_status_string(status).decode()
+        detail = lib.fp8bs_last_error_detail().decode() if status == 4 else ""
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({msg}){': ' + detail if detail else ''}")
+
+
+def _check(fn, status):
+    if status != 0:
+        raise Fp8bsError(fn, status)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _require(t, dtype, name, ndim):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.dim() != ndim or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA {dtype} tensor with {ndim} dims")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+
+
+def ld_sa_for(m: int) -> int:
+    """Row stride of the transposed activation-scale matrix: M rounded up to 4."""
+    return (m + 3) // 4 * 4
+
+
+def fp8_quant_act_1x128(x, qa=None, sa=None, stream=None):
+    """x bf16 [M, K] -> (qa uint8 [M, K] E4M3 codes, sa float32 [K/128, ld_sa]).
+
+    sa[kb, m] is the scale of row m, channels 128*kb..; ld_sa = M rounded up
+    to a multiple of 4 unless `sa` is supplied."""
+    _require(x, torch.bfloat16, "x", 2)
+    M, K = x.shape
+    if qa is None:
+        qa = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sa is None:
+        sa = torch.empty((K // 128, ld_sa_for(M)), dtype=torch.float32, device=x.device)
+    _require(qa, torch.uint8, "qa", 2)
+    _require(sa, torch.float32, "sa", 2)
+    st = lib.fp8_quant_act_1x128(_ptr(x), M, K, x.stride(0), _ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0),
+                                 _stream(stream))
+    _check("fp8_quant_act_1x128", st)
+    return qa, sa
+
+
+def fp8_quant_weight_128x128(w, qw=None, sw=None, stream=None):
+    """w bf16 [N, K] -> (qw uint8 [N, K], sw float32 [N/128, K/128]).
+    A stack of experts [G, N, K] is accepted and quantised as [G*N, K]."""
+    if isinstance(w, torch.Tensor) and w.dim() == 3:
+        G, N, K = w.shape
+        qw3 = qw if qw is not None else torch.empty((G, N, K), dtype=torch.uint8, device=w.device)
+        sw3 = sw if sw is not None else torch.empty((G, N // 128, K // 128), dtype=torch.float32, device=w.device)
+        fp8_quant_weight_128x128(w.reshape(G * N, K), qw3.view(G * N, K), sw3.view(G * N // 128, K // 128),
+                                 stream=stream)
+        return qw3, sw3
+    _require(w, torch.bfloat16, "w", 2)
+    N, K = w.shape
+    if qw is None:
+        qw = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if sw is None:
+        sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    _require(qw, torch.uint8, "qw", 2)
+    if not sw.is_contiguous():
+        raise ValueError("sw must be contiguous")
+    st = lib.fp8_quant_weight_128x128(_ptr(w), N, K, w.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
+                                      _stream(stream))
+    _check("fp8_quant_weight_128x128", st)
+    return qw, sw
+
+
+def fp8_blockscaled_gemm(qa, sa, qw, sw, y=None, stream=None):
+    """Block-scaled FP8 GEMM: Y bf16 [M, N] from qa [M, K], sa [K/128, ld_sa],
+    qw [N, K], sw [N/128, K/128]."""
+    _require(qa, torch.uint8, "qa", 2)
+    _require(qw, torch.uint8, "qw", 2)
+    _require(sa, torch.float32, "sa", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    _require(y, torch.bfloat16, "y", 2)
+    if not sw.is_contiguous():
+        raise ValueError("sw must be contiguous")
+    st = lib.fp8_blockscaled_gemm(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
+                                  _ptr(y), y.stride(0), M, N, K, _stream(stream))
+    _check("fp8_blockscaled_gemm", st)
+    return y
+
+
+def fp8_blockscaled_grouped_gemm(group_offsets, m_total, qa, sa, qw, sw, y=None, stream=None):
+    """Grouped GEMM: rows off[g]..off[g+1]-1 use expert g's weights.
+    group_offsets: CUDA int32 [G+1]; m_total: host int equal to off[G];
+    qw uint8 [G, N, K]; sw float32 [G, N/128, K/128]."""
+    if group_offsets.dtype != torch.int32 or not group_offsets.is_cuda or not group_offsets.is_contiguous():
+        raise TypeError("group_offsets must be a contiguous CUDA int32 tensor")
+    _require(qa, torch.uint8, "qa", 2)
+    _require(sa, torch.float32, "sa", 2)
+    if qw.dim() != 3 or not qw.is_contiguous() or not sw.is_contiguous():
+        raise ValueError("qw [G, N, K] and sw [G, N/128, K/128] must be contiguous")
+    G, N, K = qw.shape
+    if y is None:
+        y = torch.empty((m_total, N), dtype=torch.bfloat16, device=qa.device)
+    _require(y, torch.bfloat16, "y", 2)
+    st = lib.fp8_blockscaled_grouped_gemm(G, _ptr(group_offsets), int(m_total), _ptr(qa), qa.stride(0), _ptr(sa),
+                                          sa.stride(0), _ptr(qw), _ptr(sw), _ptr(y), y.stride(0), N, K,
+                                          _stream(stream))
+    _check("fp8_blockscaled_grouped_gemm", st)
+    return y
+
+
+def fp8bs_last_device_error(stream=None):
+    """Synchronise the stream and return (and clear) the device status code."""
+    return lib.fp8bs_last_device_error(_stream(stream))
+
+
+def fp8bs_set_wait_timeout_ns(ns: int):
+    lib.fp8bs_set_wait_timeout_ns(int(ns))
+
+
+def fp8bs_selftest_wait_timeout(ns: int, stream=None):
+    _check("fp8bs_selftest_wait_timeout", lib.fp8bs_selftest_wait_timeout(int(ns), _stream(stream)))
+
+
+def linear_forward(x, w, stream=None):
+    """The whole hot path: quantise x per 1x128 tile and w per 128x128 block,
+    then the block-scaled GEMM.  Returns (y, (qa, sa, qw, sw))."""
+    qa, sa = fp8_quant_act_1x128(x, stream=stream)
+    qw, sw = fp8_quant_weight_128x128(w, stream=stream)
+    return fp8_blockscaled_gemm(qa, sa, qw, sw, stream=stream), (qa, sa, qw, sw)

@@ -1,0 +1,51 @@
+"""Build libfp8bs.so (the C-ABI library) in-tree with nvcc for sm_103a.
+
+    python -m fp8_fine_grained_14_b300.build [--verbose]
+
+The library links the CUDA runtime statically and reaches the driver only
+through cudaGetDriverEntryPointByVersion, so it loads on hosts without a GPU
+driver (its calls then return FP8BS_ERR_CUDA).  Never built with fast math:
+the quantisation relies on IEEE division and float32 subnormals.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+SOURCES = ["api.cu", "quant.cu", "gemm.cu"]
+LIB = os.path.join(HERE, "libfp8bs.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc():
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def build(verbose: bool = False, force: bool = False) -> str:
+    srcs = [os.path.join(CSRC, s) for s in SOURCES]
+    deps = srcs + [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".cuh", ".h"))]
+    deps.append(os.path.join(ROOT, "include", "fp8bs.h"))
+    if not force and os.path.exists(LIB):
+        lib_mtime = os.path.getmtime(LIB)
+        if all(os.path.getmtime(d) <= lib_mtime for d in deps):
+            return LIB
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+           "-I", os.path.join(ROOT, "include"), "-o", LIB + ".tmp", *srcs]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if verbose or res.returncode != 0:
+        sys.stderr.write(res.stdout + res.stderr)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed ({res.returncode}): {' '.join(cmd)}")
+    os.replace(LIB + ".tmp", LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose="--verbose" in sys.argv, force=True))

@@ -1,0 +1,262 @@
+// api.cu — the C ABI declared in include/fp8bs.h: argument validation,
+// per-device state (SM count, status word), tensor-map encoding and the
+// bounded-wait self test.  Validation happens before any CUDA call, so a bad
+// argument is reported synchronously and nothing is launched.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fp8bs.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8bs {
+
+// One status word per device (each device holds its own copy of a __device__
+// variable).  Kernels record failures here; fp8bs_last_device_error reads it.
+__device__ unsigned g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s
+
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+
+struct DeviceSlot {
+  std::once_flag once;
+  DeviceInfo info;
+  cudaError_t err = cudaSuccess;
+};
+DeviceSlot g_devices[kMaxDevices];
+
+// Text of the last CUDA failure seen by a call on this host thread.
+thread_local char t_detail[256] = "";
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+void resolve_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Largest sizes the kernels index with 32-bit coordinates.
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+
+fp8bs_status cuda_failure(const char* where, cudaError_t e) {
+  std::snprintf(t_detail, sizeof(t_detail), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  return FP8BS_ERR_CUDA;
+}
+
+}  // namespace
+
+const DeviceInfo* current_device_info(cudaError_t* err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = (e != cudaSuccess) ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  DeviceSlot& slot = g_devices[dev];
+  std::call_once(slot.once, [&slot, dev]() {
+    slot.info.ordinal = dev;
+    slot.err = cudaDeviceGetAttribute(&slot.info.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (slot.err == cudaSuccess)
+      slot.err = cudaDeviceGetAttribute(&slot.info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    void* addr = nullptr;
+    if (slot.err == cudaSuccess) slot.err = cudaGetSymbolAddress(&addr, g_status_word);
+    slot.info.status = static_cast<unsigned*>(addr);
+    const unsigned zero = 0;
+    if (slot.err == cudaSuccess) slot.err = cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  });
+  if (slot.err != cudaSuccess) {
+    *err = slot.err;
+    return nullptr;
+  }
+  *err = cudaSuccess;
+  return &slot.info;
+}
+
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, resolve_encode);
+  if (g_encode == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+__global__ void selftest_wait_kernel(unsigned* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on `bar`: the bounded wait must give up.
+    if (!mbar_wait(smem_u32(&bar), 0, &abort_flag, timeout_ns)) record_status(status, kStatusTimeout);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(dev.status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8bs
+
+using fp8bs::aligned16;
+using fp8bs::cuda_failure;
+using fp8bs::kMaxDim;
+
+extern "C" {
+
+const char* fp8bs_status_string(fp8bs_status s) {
+  switch (s) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_ERR_INVALID_ARG: return "invalid argument";
+    case FP8BS_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case FP8BS_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case FP8BS_ERR_CUDA: return "CUDA error";
+    case FP8BS_ERR_TIMEOUT: return "in-kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* fp8bs_last_error_detail(void) { return fp8bs::t_detail; }
+
+void fp8bs_set_wait_timeout_ns(uint64_t timeout_ns) {
+  fp8bs::g_timeout_ns.store(timeout_ns ? timeout_ns : fp8bs::kDefaultTimeoutNs, std::memory_order_relaxed);
+}
+
+fp8bs_status fp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* qa, int64_t ldq,
+                                 float* sa, int64_t ld_sa, cudaStream_t stream) {
+  if (M < 0 || K < 0 || ldx < 0 || ldq < 0 || ld_sa < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || K > kMaxDim || M > kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K || ldq < K || ld_sa < M) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (x_bf16 == nullptr || qa == nullptr || sa == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(qa) || !aligned16(sa) || ldx % 8 != 0 || ldq % 16 != 0 || ld_sa % 4 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_quant_act_1x128(*dev, x_bf16, M, K, ldx, qa, ldq, sa, ld_sa, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_act_1x128 launch", e);
+}
+
+fp8bs_status fp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, int64_t ldw, void* qw, int64_t ldq,
+                                      float* sw, cudaStream_t stream) {
+  if (N < 0 || K < 0 || ldw < 0 || ldq < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldw < K || ldq < K) return FP8BS_ERR_INVALID_ARG;
+  if (w_bf16 == nullptr || qw == nullptr || sw == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(w_bf16) || !aligned16(qw) || !aligned16(sw) || ldw % 8 != 0 || ldq % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_quant_weight_128x128(*dev, w_bf16, N, K, ldw, qw, ldq, sw, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_weight_128x128 launch", e);
+}
+
+fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,
+                                  int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,
+                                  int64_t K, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldqw < 0 || ldy < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldqa < K || ldqw < K || ldy < N || ld_sa < M) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (qa == nullptr || sa == nullptr || qw == nullptr || sw == nullptr || y_bf16 == nullptr)
+    return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qw) || !aligned16(sw) || !aligned16(y_bf16) ||
+      ldqa % 16 != 0 || ldqw % 16 != 0 || ldy % 8 != 0 || ld_sa % 4 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_blockscaled_gemm(*dev, qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, M, N, K, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_blockscaled_gemm launch", e);
+}
+
+fp8bs_status fp8_blockscaled_grouped_gemm(int32_t G, const int32_t* group_offsets_dev, int64_t M_total,
+                                          const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                          const void* qw, const float* sw, void* y_bf16, int64_t ldy, int64_t N,
+                                          int64_t K, cudaStream_t stream) {
+  if (G <= 0 || G > 65536 || M_total < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldy < 0)
+    return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || M_total > kMaxDim ||
+      static_cast<int64_t>(G) * N > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldqa < K || ldy < N || ld_sa < M_total) return FP8BS_ERR_INVALID_ARG;
+  if (group_offsets_dev == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (M_total == 0) return FP8BS_OK;
+  if (qa == nullptr || sa == nullptr || qw == nullptr || sw == nullptr || y_bf16 == nullptr)
+    return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qw) || !aligned16(sw) || !aligned16(y_bf16) ||
+      (reinterpret_cast<uintptr_t>(group_offsets_dev) & 3u) != 0 || ldqa % 16 != 0 || ldy % 8 != 0 ||
+      ld_sa % 4 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_blockscaled_grouped_gemm(*dev, G, group_offsets_dev, M_total, qa, ldqa, sa, ld_sa, qw, sw,
+                                             y_bf16, ldy, N, K, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_blockscaled_grouped_gemm launch", e);
+}
+
+fp8bs_status fp8bs_last_device_error(cudaStream_t stream) {
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_failure("stream synchronize", e);
+  unsigned word = 0;
+  const unsigned zero = 0;
+  if ((e = cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_failure("status read", e);
+  if (word != 0 && (e = cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_failure("status clear", e);
+  switch (word) {
+    case 0: return FP8BS_OK;
+    case fp8bs::kStatusTimeout: return FP8BS_ERR_TIMEOUT;
+    case fp8bs::kStatusBadOffsets: return FP8BS_ERR_INVALID_ARG;
+  }
+  return FP8BS_ERR_CUDA;
+}
+
+fp8bs_status fp8bs_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_selftest_wait(*dev, timeout_ns, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("self-test launch", e);
+}
+
+}  // extern "C"

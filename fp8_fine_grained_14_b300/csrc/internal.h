@@ -1,0 +1,46 @@
+// internal.h — launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Arguments arrive here already validated.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8bs {
+
+struct DeviceInfo {
+  int ordinal;
+  int num_sms;
+  int max_smem_optin;
+  unsigned* status;  // device address of this device's status word
+};
+
+// Per-device facts, looked up once per device (thread-safe).  Returns nullptr
+// and sets *err when the device cannot be queried.
+const DeviceInfo* current_device_info(cudaError_t* err);
+
+uint64_t wait_timeout_ns();
+
+// Encodes a 2-D row-major tensor map; returns false on failure.
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+cudaError_t launch_quant_act_1x128(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
+                                   void* q, int64_t ldq, float* sa, int64_t ld_sa, cudaStream_t stream);
+
+cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, int64_t N, int64_t K, int64_t ldw,
+                                        void* q, int64_t ldq, float* sw, cudaStream_t stream);
+
+// Returns cudaErrorInvalidValue when a tensor map cannot be encoded.
+cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
+                                    int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
+                                    int64_t ldy, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,
+                                            int64_t M_total, const void* qa, int64_t ldqa, const float* sa,
+                                            int64_t ld_sa, const void* qw, const float* sw, void* y, int64_t ldy,
+                                            int64_t N, int64_t K, cudaStream_t stream);
+
+cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace fp8bs

@@ -1,0 +1,158 @@
+/*
+ * fp8bs.h — C ABI of the fine-grained FP8 block-scaled linear layer for
+ * B300 (sm_103a).
+ *
+ * Method: the DeepSeek-V3 FP8 mixed-precision framework as excerpted in
+ * "The Definitive Information To Deepseek":
+ *   - paragraph 3, "Figure 7 (a)": activations are grouped and scaled on 1x128
+ *     tiles (per token per 128 channels), weights on 128x128 blocks (per 128
+ *     input channels per 128 output channels);
+ *   - paragraph 2, last sentence: each group's scaling factor is derived
+ *     online and the tensor is quantised into FP8;
+ *   - paragraph 4, first sentence: the GEMM takes FP8 tensors and writes BF16;
+ *   - paragraph 1, last sentence: partial sums are promoted to a higher
+ *     precision accumulator while the next MMA proceeds.
+ * Readings of what the excerpt leaves open: FP8 is OCP E4M3FN; a group's
+ * scale is s = fl32(amax / 448) (IEEE float32 division, no flush to zero);
+ * codes are E4M3(fl32(x / s)) rounded to nearest even and saturated to +-448;
+ * an all-zero group has s = 0 and codes 0x00; promotion happens once per
+ * 128-wide K chunk with the factor sa * sw.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains them.  Base pointers must be 16-byte
+ *     aligned (FP8BS_ERR_MISALIGNED otherwise).
+ *   - Matrices are row-major; "ld" arguments are row strides in ELEMENTS.
+ *     BF16 and FP8 row strides must make 16-byte multiples (ld % 8 == 0 for
+ *     BF16, ld % 16 == 0 for FP8 codes).
+ *   - FP8 codes are OCP E4M3FN bytes (bit-compatible with torch.float8_e4m3fn).
+ *   - Activation scales are stored TRANSPOSED: sa[kb * ld_sa + m] is the scale
+ *     of row m, channels 128*kb .. 128*kb+127; ld_sa >= M and ld_sa % 4 == 0.
+ *     Weight scales are sw[nb * (K/128) + kb] for rows 128*nb.., columns 128*kb...
+ *   - Shape rules: K % 128 == 0 and K > 0; N % 128 == 0 and N > 0;
+ *     M >= 0 is arbitrary (M == 0 is a no-op).  Violations return
+ *     FP8BS_ERR_UNSUPPORTED_SHAPE (or FP8BS_ERR_INVALID_ARG for negative sizes,
+ *     short strides and null pointers) before anything is launched.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *     returns after validation and launch.  A launch failure returns
+ *     FP8BS_ERR_CUDA (fp8bs_last_error_detail() names the CUDA error).
+ *     Kernel waits are bounded; a wait that gives up records
+ *     FP8BS_ERR_TIMEOUT in a per-device status word, which
+ *     fp8bs_last_device_error() reports.
+ *   - No CPU fallback exists: without a usable CUDA device the calls fail.
+ *   - Thread safety: calls may be made concurrently from several host threads.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8BS_OK = 0,
+  FP8BS_ERR_INVALID_ARG = 1,       /* null pointer, negative size, short stride or bad group offsets */
+  FP8BS_ERR_MISALIGNED = 2,        /* pointer or row stride breaks the 16-byte rules above */
+  FP8BS_ERR_UNSUPPORTED_SHAPE = 3, /* K or N not a positive multiple of 128, or sizes too large */
+  FP8BS_ERR_CUDA = 4,              /* a CUDA runtime/driver call or a launch failed */
+  FP8BS_ERR_TIMEOUT = 5            /* a bounded in-kernel wait gave up (reported asynchronously) */
+} fp8bs_status;
+
+/*
+ * 1x128 activation quantisation ("Figure 7 (a)" item (1); online scaling of
+ * paragraph 2).
+ *   x_bf16 : [M, K] BF16, row stride ldx (elements).
+ *   qa     : [M, K] E4M3 codes out, row stride ldq (bytes).
+ *   sa     : [K/128, ld_sa] FP32 scales out, sa[kb*ld_sa + m].
+ * Columns m >= M of sa are left untouched.
+ */
+fp8bs_status fp8_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                 void* qa, int64_t ldq, float* sa, int64_t ld_sa,
+                                 cudaStream_t stream);
+
+/*
+ * 128x128 weight quantisation ("Figure 7 (a)" item (2)).
+ *   w_bf16 : [N, K] BF16 (row = output channel), row stride ldw.
+ *   qw     : [N, K] E4M3 codes out, row stride ldq.
+ *   sw     : [N/128, K/128] FP32 scales out, row-major, contiguous.
+ * A stack of G expert weights [G, N, K] can be passed as one [G*N, K] matrix:
+ * blocks never straddle experts because N % 128 == 0.
+ */
+fp8bs_status fp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, int64_t ldw,
+                                      void* qw, int64_t ldq, float* sw, cudaStream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM with per-128-K-chunk promotion (paragraphs 1 and 4):
+ *   Y[m, n] = bf16( sum_kb sa[kb*ld_sa + m] * sw[(n/128)*(K/128) + kb]
+ *                   * sum_{k in chunk kb} dec(qa[m, k]) * dec(qw[n, k]) ).
+ *   qa : [M, K] codes, row stride ldqa (bytes);  qw : [N, K] codes, stride ldqw.
+ *   y  : [M, N] BF16 out, row stride ldy (elements).
+ * Chunk products accumulate in FP32 tensor memory; each chunk is scaled and
+ * added to an FP32 register accumulator; the result is rounded to BF16
+ * (round to nearest even).
+ */
+fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                  const void* qw, int64_t ldqw, const float* sw,
+                                  void* y_bf16, int64_t ldy,
+                                  int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * Grouped (per-expert) block-scaled GEMM for MoE row groups.  Rows
+ * off[g] .. off[g+1]-1 of qa, sa and y belong to expert g and are multiplied
+ * by expert g's weights:
+ *   group_offsets_dev : DEVICE int32 [G+1], off[0] == 0, non-decreasing,
+ *                       off[G] == M_total (checked on the device: a bad table
+ *                       records FP8BS_ERR_INVALID_ARG in the status word and
+ *                       the offending groups are skipped).
+ *   M_total           : host copy of off[G] (sizes the launch; 0 is a no-op).
+ *   qa [M_total, K] (stride ldqa), sa [K/128, ld_sa] with ld_sa >= M_total,
+ *   qw [G, N, K] contiguous codes, sw [G, N/128, K/128] contiguous scales,
+ *   y [M_total, N] BF16 (stride ldy).  Empty groups are allowed.
+ *   1 <= G <= 65536.
+ */
+fp8bs_status fp8_blockscaled_grouped_gemm(int32_t G, const int32_t* group_offsets_dev, int64_t M_total,
+                                          const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                          const void* qw, const float* sw,
+                                          void* y_bf16, int64_t ldy,
+                                          int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * Text naming the CUDA error (and the step) behind the last FP8BS_ERR_CUDA
+ * returned to the calling host thread; "" if none.  Valid until the thread's
+ * next call into the library.
+ */
+const char* fp8bs_last_error_detail(void);
+
+/* Static, human-readable name of a status code. */
+const char* fp8bs_status_string(fp8bs_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns FP8BS_OK, FP8BS_ERR_TIMEOUT, FP8BS_ERR_INVALID_ARG (a bad
+ * group-offset table) or FP8BS_ERR_CUDA (the synchronisation failed).
+ */
+fp8bs_status fp8bs_last_device_error(cudaStream_t stream);
+
+/*
+ * Limit, in nanoseconds, of every bounded in-kernel wait launched after the
+ * call (default 1e9 = 1 s; 0 restores the default).  Process-wide.
+ */
+void fp8bs_set_wait_timeout_ns(uint64_t timeout_ns);
+
+/*
+ * Self-test of the bounded-wait path: launches one warp that waits on a
+ * barrier nothing will ever signal, with a limit of `timeout_ns`.  The wait
+ * gives up, records FP8BS_ERR_TIMEOUT in the status word and the kernel
+ * returns; the context stays usable.  No counterpart in the method; it exists
+ * so failure detection can be exercised without faulting or hanging a GPU.
+ */
+fp8bs_status fp8bs_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,91 @@
+"""Parity of the grouped (per-expert) block-scaled GEMM with the CPU oracle.
+
+MoE row groups: rows off[g]..off[g+1]-1 use expert g's 128x128-quantised
+weights; activations are quantised per 1x128 tile over the concatenated rows
+("The Definitive Information To Deepseek", "Figure 7 (a)").  Empty and
+ragged groups are part of the contract.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_fine_grained_14_b300 as fb
+import oracle
+from fp8_fine_grained_14_b300 import workloads
+from helpers import assert_codes_equal, assert_gemm_close, assert_scales_equal, f32, sample_rows, u8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _grouped_gpu(offsets, x, w):
+    xd, wd = x.to(DEV), w.to(DEV)
+    qa, sa = fb.fp8_quant_act_1x128(xd)
+    qw, sw = fb.fp8_quant_weight_128x128(wd)
+    y = fb.fp8_blockscaled_grouped_gemm(offsets.to(DEV), int(offsets[-1]), qa, sa, qw, sw)
+    torch.cuda.synchronize()
+    return y, qa, sa, qw, sw
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([3, 0, 130, 1, 0, 257], 256, 256),
+    ([128, 128], 128, 384),
+    ([0, 0, 1], 384, 128),
+    ([500], 512, 256),
+    ([77, 300, 0, 129, 5, 64, 200, 1], 1024, 512),  # 256-wide tiles across ragged groups
+])
+def test_grouped_small(counts, N, K):
+    G = len(counts)
+    offsets = workloads.grouped_offsets(counts)
+    x, _ = workloads.dense_inputs(int(offsets[-1]), 128, K, seed=G + N)
+    _, w = workloads.dense_inputs(1, G * N, K, seed=G + N + 1)
+    w = w.reshape(G, N, K)
+    y, qa, sa, qw, sw = _grouped_gpu(offsets, x, w)
+    assert fb.fp8bs_last_device_error() == 0
+    qa_r, sa_r = oracle.quant_act_1x128(f32(x))
+    qw_r, sw_r = oracle.quant_weight_128x128(f32(w).reshape(G * N, K))
+    assert_codes_equal(u8(qa), qa_r, "qa")
+    assert_scales_equal(f32(sa)[:, : int(offsets[-1])], sa_r, "sa")
+    assert_codes_equal(u8(qw).reshape(G * N, K), qw_r, "qw")
+    assert_scales_equal(f32(sw).reshape(G * N // 128, K // 128), sw_r, "sw")
+    y_ref = oracle.blockscaled_grouped_gemm(offsets.numpy(), qa_r, sa_r, qw_r.reshape(G, N, K),
+                                            sw_r.reshape(G, N // 128, K // 128))
+    assert_gemm_close(f32(y), y_ref)
+
+
+def test_grouped_bad_offsets_reported():
+    """A decreasing offset table is detected on the device and reported."""
+    N, K = 128, 128
+    offsets = torch.tensor([0, 100, 50, 150], dtype=torch.int32)
+    x, _ = workloads.dense_inputs(150, 128, K, seed=1)
+    _, w = workloads.dense_inputs(1, 3 * N, K, seed=2)
+    _grouped_gpu(offsets, x, w.reshape(3, N, K))
+    assert fb.fp8bs_last_device_error() == 1  # FP8BS_ERR_INVALID_ARG
+    assert fb.fp8bs_last_device_error() == 0  # cleared by the read
+
+
+def test_grouped_full_size_sampled():
+    """The grouped MoE configuration (64 experts, 65536 routed rows, N=2048,
+    K=7168) in the benchmark's launch configuration; oracle on sampled rows
+    of sampled groups (every 128-row tile) against all of the group's columns."""
+    c = workloads.CONFIGS["grouped"]
+    offsets, x, w = workloads.grouped_inputs(**{k: c[k] for k in ("tokens", "topk", "G", "N", "K")})
+    y, qa, sa, qw, sw = _grouped_gpu(offsets, x, w)
+    assert fb.fp8bs_last_device_error() == 0
+    off = offsets.numpy()
+    G, N, K = w.shape
+    rng = np.random.default_rng(3)
+    groups = sorted(set([0, G - 1]) | set(rng.choice(G, 4, replace=False).tolist()))
+    for g in groups:
+        r0, r1 = int(off[g]), int(off[g + 1])
+        if r1 == r0:
+            continue
+        rows = r0 + sample_rows(r1 - r0, 24, seed=g)
+        qa_r, sa_r = oracle.quant_act_1x128(f32(x[torch.as_tensor(rows)]))
+        qw_r, sw_r = oracle.quant_weight_128x128(f32(w[g]))
+        assert_codes_equal(u8(qa[torch.as_tensor(rows, device=DEV)]), qa_r, f"qa group {g}")
+        assert_scales_equal(f32(sa)[:, rows], sa_r, f"sa group {g}")
+        assert_codes_equal(u8(qw[g]), qw_r, f"qw group {g}")
+        assert_scales_equal(f32(sw[g]), sw_r, f"sw group {g}")
+        y_ref = oracle.blockscaled_gemm(qa_r, sa_r, qw_r, sw_r)
+        assert_gemm_close(f32(y[torch.as_tensor(rows, device=DEV)]), y_ref, what=f"group {g}")

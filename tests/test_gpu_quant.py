@@ -1,0 +1,123 @@
+"""Bit-exact parity of the CUDA quantisation kernels with the CPU oracle.
+
+1x128 activation tiles and 128x128 weight blocks ("The Definitive
+Information To Deepseek", paragraph 3, "Figure 7 (a)"); per-group online
+scale (paragraph 2).  Codes and scales must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_fine_grained_14_b300 as fb
+import oracle
+from fp8_fine_grained_14_b300 import workloads
+from helpers import assert_codes_equal, assert_scales_equal, f32, sample_blocks, sample_rows, u8
+from oracle_pins import exact_tie_groups
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _act_parity(x_cpu, rows=None):
+    x = x_cpu.to(DEV)
+    qa, sa = fb.fp8_quant_act_1x128(x)
+    torch.cuda.synchronize()
+    M = x_cpu.shape[0]
+    rows = np.arange(M) if rows is None else rows
+    qa_ref, sa_ref = oracle.quant_act_1x128(f32(x_cpu)[rows])
+    assert_codes_equal(u8(qa)[rows], qa_ref, "qa")
+    assert_scales_equal(f32(sa)[:, rows], sa_ref, "sa")
+    return qa, sa
+
+
+def _weight_parity(w_cpu, blocks=None):
+    w = w_cpu.to(DEV)
+    qw, sw = fb.fp8_quant_weight_128x128(w)
+    torch.cuda.synchronize()
+    if w_cpu.dim() == 3:
+        G, N, K = w_cpu.shape
+        w2, qw2, sw2 = w_cpu.reshape(G * N, K), qw.reshape(G * N, K), sw.reshape(G * N // 128, K // 128)
+    else:
+        w2, qw2, sw2 = w_cpu, qw, sw
+    NB = w2.shape[0] // 128
+    blocks = np.arange(NB) if blocks is None else blocks
+    rows = np.concatenate([np.arange(b * 128, b * 128 + 128) for b in blocks])
+    qw_ref, sw_ref = oracle.quant_weight_128x128(f32(w2)[rows])
+    assert_codes_equal(u8(qw2)[rows], qw_ref, "qw")
+    assert_scales_equal(f32(sw2)[blocks], sw_ref, "sw")
+    return qw, sw
+
+
+@pytest.mark.parametrize("M,K", [(128, 256), (1, 128), (3, 384), (127, 128), (129, 640), (300, 896), (1000, 1280)])
+def test_act_quant_shapes(M, K):
+    x, _ = workloads.dense_inputs(M, 128, K, seed=M + K)
+    _act_parity(x)
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 256), (384, 640), (1024, 1152)])
+def test_weight_quant_shapes(N, K):
+    _, w = workloads.dense_inputs(1, N, K, seed=N + K)
+    _weight_parity(w)
+
+
+def test_act_quant_exact_ties_and_edges():
+    """Exact E4M3 midpoint quotients, all-zero groups (with -0), tiny
+    (subnormal-scale) and huge groups, negative values rounding to zero."""
+    # exact-tie rows: BF16 holds m*s exactly for these short-mantissa scales
+    x_ties, _ = exact_tie_groups(scales=(1.5, 1.75, 1.25, 0.75 * 2.0 ** -20, 1.5 * 2.0 ** 30))
+    ties_bf16 = torch.from_numpy(x_ties).to(torch.bfloat16)
+    assert np.array_equal(f32(ties_bf16), x_ties), "tie inputs must be BF16-exact"
+    rows = [x_ties]
+    rng = np.random.default_rng(0)
+    z = np.zeros((1, 128), dtype=np.float32)
+    z[0, 5] = -0.0
+    rows.append(z)
+    for e in (-133, -126, -120, -60, 60, 120):
+        rows.append((rng.standard_normal((1, 128)) * 2.0 ** e).astype(np.float32))
+    mixed = rng.standard_normal((1, 128)).astype(np.float32)
+    mixed[0, :10] = -(2.0 ** -20)  # far below the group's E4M3 resolution: -0 codes
+    rows.append(mixed)
+    x = torch.from_numpy(np.concatenate(rows)).to(torch.bfloat16)
+    qa, _ = _act_parity(x)
+    assert u8(qa)[len(x_ties), 5] == 0x00  # -0 in an all-zero group codes as +0
+    assert np.all(u8(qa)[-1, :10] == 0x80)
+
+
+def test_weight_quant_edges():
+    rng = np.random.default_rng(1)
+    w = (rng.standard_normal((512, 256)) * 0.02).astype(np.float32)
+    w[0:128, 0:128] = 0.0                # all-zero block
+    w[128:256, 128:256] *= 2.0 ** -126   # tiny block (subnormal scale)
+    w[256:384, 0:128] *= 2.0 ** 100      # huge block
+    w[384:512, 128:256] = 448.0 * 1.5    # constant block, s = 1.5
+    _weight_parity(torch.from_numpy(w).to(torch.bfloat16))
+
+
+def test_act_quant_strided_input_and_ld_sa():
+    """Row strides larger than K and a padded scale stride."""
+    x_full, _ = workloads.dense_inputs(200, 128, 512, seed=3)
+    xd = x_full.to(DEV)[:, :384]  # ldx = 512, K = 384
+    qa = torch.full((200, 400), 0x55, dtype=torch.uint8, device=DEV)[:, :384]  # ldq = 400
+    sa = torch.full((3, 208), -1.0, dtype=torch.float32, device=DEV)
+    fb.fp8_quant_act_1x128(xd, qa=qa, sa=sa)
+    torch.cuda.synchronize()
+    qa_ref, sa_ref = oracle.quant_act_1x128(f32(x_full)[:, :384])
+    assert_codes_equal(u8(qa), qa_ref, "qa")
+    assert_scales_equal(f32(sa)[:, :200], sa_ref, "sa")
+    assert np.all(f32(sa)[:, 200:] == -1.0), "columns >= M of sa must be untouched"
+
+
+@pytest.mark.parametrize("name", ["up", "down", "decode"])
+def test_quant_full_size_sampled(name):
+    """Full-size configurations, launched as the benchmark launches them;
+    oracle on sampled rows (every 128-row tile) and sampled weight blocks."""
+    x, w = workloads.config_inputs(name)
+    _act_parity(x, rows=sample_rows(x.shape[0], 256, seed=1))
+    _weight_parity(w, blocks=sample_blocks(w.shape[0] // 128, 6, seed=2))
+
+
+def test_quant_grouped_full_size_sampled():
+    c = workloads.CONFIGS["grouped"]
+    offsets, x, w = workloads.grouped_inputs(**{k: c[k] for k in ("tokens", "topk", "G", "N", "K")})
+    _act_parity(x, rows=sample_rows(x.shape[0], 512, seed=4))
+    _weight_parity(w, blocks=sample_blocks(w.shape[0] * w.shape[1] // 128, 8, seed=5))
