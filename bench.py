@@ -1,0 +1,629 @@
+#!/usr/bin/env python3
+"""Benchmark of the fine-grained FP8 block-scaled linear layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config up|down|grouped|decode|tiny]
+                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+
+One step is one pass of the whole hot path over one batch of synthetic input
+already resident in HBM:
+  * up / down / tiny : 1x128 activation quantisation of X, 128x128 weight
+                       quantisation of W, block-scaled GEMM -> Y (BF16);
+  * grouped          : the same over 64 expert row groups, grouped GEMM;
+  * decode           : activation quantisation + GEMM (W quantised once,
+                       before timing, as the workload specifies).
+The default workload is the up-projection X[4096, 7168] x W[18432, 7168].
+
+Printed (rank 0, one JSON line): whole-job TFLOP/s (2MNK per step, all
+ranks, the step's quantisation included), per-kernel CUDA-event times, the
+roofline of the dominant kernel against the measured peaks, SM clocks sampled
+during the timed region, an end-to-end figure through the C ABI with pinned
+host buffers (host->device inputs and device->host Y inside the timed
+region), and the CPU oracle timed on a bounded sample (rank 0, N = 1).
+
+With --impl reference the CPU oracle itself is timed, one bounded sample of
+the workload per step, on this host's cores (rank 0 only).
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize(); the maximum over ranks is reported.  No L2 flush:
+every step's working set (inputs, codes, scales, output) is several times the
+126 MB L2.  Multi-GPU runs are independent replicas (weak scaling): the
+linear layer needs no exchange between ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fp8_fine_grained_14_b300 import workloads  # noqa: E402
+
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "fp8_fine_grained_14_b300", "csrc")
+
+# Dense FP8 tensor peak = measured BF16 peak x 2 (nominal dense ratio on B300:
+# 4.5 PFLOP/s FP8 vs 2.25 PFLOP/s BF16).
+FP8_PER_BF16 = 2.0
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny linear: X bf16 [128,256] ~N(0,1), W bf16 [256,256] ~N(0,0.02); "
+            "1x128 act quant + 128x128 weight quant + block-scaled GEMM -> Y bf16 [128,256]",
+    "up": "up-projection: X bf16 [4096,7168] ~N(0,1), W bf16 [18432,7168] ~N(0,0.02); "
+          "1x128 act quant + 128x128 weight quant (E4M3, FP32 scales) + FP32-promoted block-scaled "
+          "GEMM -> Y bf16 [4096,18432]",
+    "down": "down-projection with outliers: X bf16 [4096,18432] ~N(0,1) with 18 channels x100, "
+            "W bf16 [7168,18432] ~N(0,0.02); act + weight quant + block-scaled GEMM -> Y bf16 [4096,7168]",
+    "grouped": "grouped MoE GEMM: 8192 tokens x top-8 over 64 experts (65536 rows), X bf16 [65536,7168], "
+               "W bf16 [64,2048,7168]; act + weight quant + grouped block-scaled GEMM",
+    "decode": "decode-shaped skinny GEMM: X bf16 [64,7168] ~N(0,1), W [18432,7168] pre-quantised 128x128 "
+              "E4M3; act quant + block-scaled GEMM",
+}
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work per kernel launch (each operand read once, each output
+# written once; re-reads caused by tiling are not counted).
+# ---------------------------------------------------------------------------
+def act_quant_bytes(M, K):
+    return 2 * M * K + M * K + 4 * M * (K // 128)
+
+
+def weight_quant_bytes(N, K):
+    return 2 * N * K + N * K + 4 * (N // 128) * (K // 128)
+
+
+def gemm_bytes(M, N, K, G=1):
+    return M * K + G * N * K + 4 * M * (K // 128) + 4 * G * (N // 128) * (K // 128) + 2 * M * N
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK}, "measured"
+    except (OSError, ValueError, KeyError):
+        return dict(FALLBACK), "fallback"
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "gemm": ["gemm.cu", "ptx.cuh"],
+    "grouped_gemm": ["gemm.cu", "ptx.cuh"],
+    "act_quant": ["quant.cu", "ptx.cuh"],
+    "weight_quant": ["quant.cu", "ptx.cuh"],
+}
+
+
+def profiled_traffic(kernel, config):
+    """DRAM bytes per launch from a committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel source has changed
+    since the counters were taken.  Summaries carry lines
+    `kernel: <k>`, `config: <c>`, `source_sha256_16: <digest>` and
+    `dram_bytes_per_launch: <bytes>`."""
+    if not os.path.isdir(PROFILES):
+        return None
+    want = source_digest(KERNEL_SOURCES[kernel])
+    for name in sorted(os.listdir(PROFILES)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(PROFILES, name)) as f:
+            text = f.read()
+        fields = dict(re.findall(r"^\s*[-*]?\s*`?(kernel|config|source_sha256_16|dram_bytes_per_launch)`?:\s*`?([\w.+-]+)`?",
+                                 text, flags=re.M))
+        if fields.get("kernel") == kernel and fields.get("config") == config:
+            if fields.get("source_sha256_16") == want and "dram_bytes_per_launch" in fields:
+                return int(float(fields["dram_bytes_per_launch"]))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, period_ms=20):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def warm(self):
+        """Wait (bounded) for the sampler's first line so the timed region is covered."""
+        if self.proc is None:
+            return
+        line = self.proc.stdout.readline()
+        if line:
+            self.first = line
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas; the barrier and max-over-ranks only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value, device):
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# Workload setup
+# ---------------------------------------------------------------------------
+def make_inputs(name, seed):
+    """CPU tensors of the workload (seeded; see fp8_fine_grained_14_b300.workloads)."""
+    if name == "grouped":
+        c = workloads.CONFIGS["grouped"]
+        offsets, x, w = workloads.grouped_inputs(**{k: c[k] for k in ("tokens", "topk", "G", "N", "K")}, seed=seed)
+        return {"offsets": offsets, "x": x, "w": w}
+    x, w = workloads.config_inputs(name, seed=seed)
+    return {"x": x, "w": w}
+
+
+def shapes(name, inp):
+    if name == "grouped":
+        G, N, K = inp["w"].shape
+        return dict(M=inp["x"].shape[0], N=N, K=K, G=G)
+    return dict(M=inp["x"].shape[0], N=inp["w"].shape[0], K=inp["x"].shape[1], G=1)
+
+
+class Step:
+    """Pre-marshalled C-ABI calls of one step on one stream."""
+
+    def __init__(self, name, inp, device, stream, fb):
+        self.name = name
+        self.fb = fb
+        self.lib = fb.binding.lib
+        self.stream = stream
+        s = shapes(name, inp)
+        self.M, self.N, self.K, self.G = s["M"], s["N"], s["K"], s["G"]
+        M, N, K, G = self.M, self.N, self.K, self.G
+        self.x = inp["x"].to(device)
+        self.w = inp["w"].to(device)
+        self.qa = torch.empty((M, K), dtype=torch.uint8, device=device)
+        self.sa = torch.empty((K // 128, fb.ld_sa_for(M)), dtype=torch.float32, device=device)
+        self.qw = torch.empty((G * N, K), dtype=torch.uint8, device=device)
+        self.sw = torch.empty((G * N // 128, K // 128), dtype=torch.float32, device=device)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.offsets = inp["offsets"].to(device) if "offsets" in inp else None
+        self.kernels = ["act_quant"] + ([] if name == "decode" else ["weight_quant"]) + \
+            (["grouped_gemm"] if name == "grouped" else ["gemm"])
+        if name == "decode":
+            with torch.cuda.stream(stream):
+                self.weight_quant()  # pre-quantised weights: outside the timed region
+            stream.synchronize()
+
+    def _st(self):
+        import ctypes
+
+        return ctypes.c_void_p(self.stream.cuda_stream)
+
+    def _check(self, fn, status):
+        if status != 0:
+            raise self.fb.Fp8bsError(fn, status)
+
+    def act_quant(self):
+        p = lambda t: t.data_ptr()  # noqa: E731
+        self._check("fp8_quant_act_1x128", self.lib.fp8_quant_act_1x128(
+            p(self.x), self.M, self.K, self.x.stride(0), p(self.qa), self.qa.stride(0), p(self.sa),
+            self.sa.stride(0), self._st()))
+
+    def weight_quant(self):
+        p = lambda t: t.data_ptr()  # noqa: E731
+        self._check("fp8_quant_weight_128x128", self.lib.fp8_quant_weight_128x128(
+            p(self.w), self.G * self.N, self.K, self.K, p(self.qw), self.qw.stride(0), p(self.sw), self._st()))
+
+    def gemm(self):
+        p = lambda t: t.data_ptr()  # noqa: E731
+        self._check("fp8_blockscaled_gemm", self.lib.fp8_blockscaled_gemm(
+            p(self.qa), self.qa.stride(0), p(self.sa), self.sa.stride(0), p(self.qw), self.qw.stride(0),
+            p(self.sw), p(self.y), self.y.stride(0), self.M, self.N, self.K, self._st()))
+
+    def grouped_gemm(self):
+        p = lambda t: t.data_ptr()  # noqa: E731
+        self._check("fp8_blockscaled_grouped_gemm", self.lib.fp8_blockscaled_grouped_gemm(
+            self.G, p(self.offsets), self.M, p(self.qa), self.qa.stride(0), p(self.sa), self.sa.stride(0),
+            p(self.qw), p(self.sw), p(self.y), self.y.stride(0), self.N, self.K, self._st()))
+
+    def run(self, events=None):
+        """One step; if `events` is a list, an event is recorded after each kernel."""
+        for k in self.kernels:
+            getattr(self, k)()
+            if events is not None:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(self.stream)
+                events.append(ev)
+
+    def flops(self):
+        return 2 * self.M * self.N * self.K
+
+    def algorithmic(self, kernel):
+        M, N, K, G = self.M, self.N, self.K, self.G
+        if kernel == "act_quant":
+            return act_quant_bytes(M, K), "hbm"
+        if kernel == "weight_quant":
+            return weight_quant_bytes(G * N, K), "hbm"
+        if self.name == "decode":
+            return gemm_bytes(M, N, K), "hbm"
+        return 2 * M * N * K, "tensor"
+
+
+def time_device(step, stream, steps, warmup, dist, device):
+    for _ in range(warmup):
+        with torch.cuda.stream(stream):
+            step.run()
+    torch.cuda.synchronize(device)
+    if step.fb.fp8bs_last_device_error(stream) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    sampler = ClockSampler(device.index)
+    sampler.warm()
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    events = []
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step.run(events)
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    sampler.stop()
+    total_ms = start.elapsed_time(end)
+    nk = len(step.kernels)
+    per_kernel = {k: 0.0 for k in step.kernels}
+    prev = start
+    for i, ev in enumerate(events):
+        per_kernel[step.kernels[i % nk]] += prev.elapsed_time(ev)
+        prev = ev
+    per_kernel = {k: v / steps for k, v in per_kernel.items()}
+    status = step.fb.fp8bs_last_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device status word {status} after the timed region")
+    return total_ms, per_kernel, sampler.summary()
+
+
+def time_e2e(name, inp, step, stream, steps, warmup, device):
+    """Same metric through the C ABI from pinned host buffers: per step the
+    inputs go host->device and Y comes back device->host inside the timed region."""
+    hx = inp["x"].pin_memory()
+    hw = inp["w"].pin_memory() if name != "decode" else None
+    hy = torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()
+    h2d = hx.numel() * hx.element_size() + (hw.numel() * hw.element_size() if hw is not None else 0)
+    d2h = hy.numel() * hy.element_size()
+
+    def one():
+        with torch.cuda.stream(stream):
+            step.x.copy_(hx, non_blocking=True)
+            if hw is not None:
+                step.w.copy_(hw.view(step.w.shape), non_blocking=True)
+            step.run()
+            hy.copy_(step.y, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    ms = start.elapsed_time(end) / steps
+    return ms, wall, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (test infrastructure; only this leg of the benchmark
+# executes the oracle)
+# ---------------------------------------------------------------------------
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        return 1
+
+
+def oracle_sample(name, inp, m_rows, n_rows):
+    """Run the oracle's whole path on rows [0, m_rows) of X and the first
+    n_rows (a multiple of 128) weight rows (of expert 0 when grouped).
+    Returns (seconds, FLOPs of the sample)."""
+    import oracle
+
+    x = inp["x"][:m_rows].float().numpy()
+    w = inp["w"][0] if name == "grouped" else inp["w"]
+    w = w[:n_rows].float().numpy()
+    K = x.shape[1]
+    t0 = time.perf_counter()
+    qa, sa = oracle.quant_act_1x128(x)
+    if name == "decode":
+        qw, sw = _decode_prequant_cache(w)
+    else:
+        qw, sw = oracle.quant_weight_128x128(w)
+    oracle.blockscaled_gemm(qa, sa, qw, sw)
+    return time.perf_counter() - t0, 2 * m_rows * n_rows * K
+
+
+_PREQ = {}
+
+
+def _decode_prequant_cache(w):
+    import oracle
+
+    key = (w.shape, float(w[0, 0]))
+    if key not in _PREQ:
+        _PREQ[key] = oracle.quant_weight_128x128(w)
+    return _PREQ[key]
+
+
+def cpu_baseline(name, inp, target_s=12.0):
+    M = inp["x"].shape[0]
+    N = inp["w"].shape[-2]
+    m_rows = min(M, 512)
+    n_rows = min(N, 1024)
+    t, fl = oracle_sample(name, inp, m_rows, n_rows)
+    reps = max(1, min(20, int(target_s / max(t, 1e-3))))
+    tot_t, tot_f = t, fl
+    for _ in range(reps - 1):
+        t, fl = oracle_sample(name, inp, m_rows, n_rows)
+        tot_t += t
+        tot_f += fl
+    what = "expert 0's " if name == "grouped" else ""
+    return {
+        "value": tot_f / tot_t / 1e12,
+        "unit": "TFLOP/s",
+        "cores": oracle_threads(),
+        "kind": "oracle",
+        "sample": (f"CPU oracle (numpy, float64 GEMM through BLAS) on X[:{m_rows}] and {what}W[:{n_rows}] with the "
+                   f"full K, quantisation{' of X' if name == 'decode' else ''} and GEMM, {reps} repetitions "
+                   f"({tot_t:.1f} s); value = sample FLOPs / sample time"),
+    }
+
+
+# ---------------------------------------------------------------------------
+# Arms
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    name = args.config
+    inp = make_inputs(name, seed=0)
+    M = inp["x"].shape[0]
+    N = inp["w"].shape[-2]
+    # size each step's sample so that warm-up + steps end within ~150 s
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n_rows = min(N, 128)
+    m_rows = min(M, 8)
+    t, _ = oracle_sample(name, inp, m_rows, n_rows)
+    while m_rows * 2 <= min(M, 512) and t * 2 <= budget:
+        m_rows *= 2
+        t, _ = oracle_sample(name, inp, m_rows, n_rows)
+    for _ in range(args.warmup):
+        oracle_sample(name, inp, m_rows, n_rows)
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        _, fl = oracle_sample(name, inp, m_rows, n_rows)
+        flops += fl
+    elapsed = time.perf_counter() - t0
+    value = flops / elapsed / 1e12
+    unit = "TFLOP/s"
+    line = {
+        "impl": "reference",
+        "metric": "block-scaled FP8 GEMM TFLOPS (incl. quant) vs FP8 peak; quant GB/s vs HBM",
+        "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[name], "M": M, "N": N, "K": inp["x"].shape[1],
+                   "parallelism": "rank 0 only (CPU)"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle_threads(), "kind": "oracle",
+                         "sample": f"per step: CPU oracle quantisation + GEMM on X[:{m_rows}] and W[:{n_rows}] "
+                                   f"with the full K; value = sample FLOPs / time"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def load_library():
+    try:
+        import fp8_fine_grained_14_b300 as fb
+
+        fb.binding  # noqa: B018  (loads libfp8bs.so; raises when it is missing)
+        return fb
+    except ImportError:
+        from fp8_fine_grained_14_b300 import build
+
+        build.build()
+        import fp8_fine_grained_14_b300 as fb
+
+        fb.binding  # noqa: B018
+        return fb
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    fb = load_library()
+    name = args.config
+    inp = make_inputs(name, seed=rank)
+    stream = torch.cuda.Stream(device)
+    step = Step(name, inp, device, stream, fb)
+
+    total_ms, per_kernel, clocks = time_device(step, stream, args.steps, args.warmup, dist, device)
+    total_ms = max_over_ranks(dist, total_ms, device)
+    ms_per_step = total_ms / args.steps
+    flops = step.flops()
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    kern = {}
+    for k, ms in per_kernel.items():
+        units, bound = step.algorithmic(k)
+        if bound == "tensor":
+            peak = peaks["bf16_tflops"] * FP8_PER_BF16
+            achieved = units / (ms * 1e-3) / 1e12
+            unit = "TFLOP/s"
+        else:
+            peak = peaks["hbm_gbs"]
+            achieved = units / (ms * 1e-3) / 1e9
+            unit = "GB/s"
+        kern[k] = {"us": ms * 1e3, "achieved": achieved, "unit": unit, "frac": achieved / peak, "peak": peak,
+                   "bound": bound, "algorithmic": units}
+    dominant = max(per_kernel, key=per_kernel.get)
+    d = kern[dominant]
+    roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": profiled_traffic(dominant, name),
+                "peak_source": (f"{peak_src} " + ("bf16 burst x 2 (dense FP8/BF16 nominal ratio)"
+                                                  if d["bound"] == "tensor" else "HBM copy"))}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        ms, wall, h2d, d2h = time_e2e(name, inp, step, stream, e2e_steps, 2, device)
+        ms = max_over_ranks(dist, ms, device)
+        e2e = {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(name, inp)
+
+    if rank == 0:
+        M, N, K = step.M, step.N, step.K
+        line = {
+            "metric": "block-scaled FP8 GEMM TFLOPS (incl. quant) vs FP8 peak; quant GB/s vs HBM",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 (f32 accumulate, bf16 out)", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[name], "name": name, "M": M, "N": N, "K": K, "G": step.G,
+                       "step": " + ".join(step.kernels), "l2": "no flush: inputs larger than L2 "
+                       "(step working set > 126 MB)", "parallelism": f"replicas x{world}"},
+            "roofline": roofline,
+            "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                        for k, v in kern.items()},
+            "tflops_gemm_only": flops / (per_kernel[step.kernels[-1]] * 1e-3) / 1e12,
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": len(step.kernels) * args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="up", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps; the number is not a valid measurement", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
