@@ -406,12 +406,21 @@ def time_e2e(name, inp, step, stream, steps, warmup, device):
 # executes the oracle)
 # ---------------------------------------------------------------------------
 def oracle_threads():
+    """Threads the oracle's BLAS pool actually uses (its quantisation runs on
+    one thread)."""
     try:
         from threadpoolctl import threadpool_info
 
         return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
     except Exception:
         return 1
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def oracle_sample(name, inp, m_rows, n_rows):
@@ -466,7 +475,8 @@ def cpu_baseline(name, inp, target_s=12.0):
         "kind": "oracle",
         "sample": (f"CPU oracle (numpy, float64 GEMM through BLAS) on X[:{m_rows}] and {what}W[:{n_rows}] with the "
                    f"full K, quantisation{' of X' if name == 'decode' else ''} and GEMM, {reps} repetitions "
-                   f"({tot_t:.1f} s); value = sample FLOPs / sample time"),
+                   f"({tot_t:.1f} s); value = sample FLOPs / sample time; quantisation on 1 thread, BLAS on "
+                   f"{oracle_threads()} of the {host_cores()} cores in this process's affinity mask"),
     }
 
 
