@@ -14,8 +14,10 @@
 //               (K = 32 each) per chunk into TMEM buffer (chunk & 1), then
 //               tcgen05.commit to free the smem stage and publish the chunk
 //   warps 2..3  idle (their warpgroup gives registers to the promotion warps)
-//   warps 4..11 promotion: tcgen05.ld the chunk (one row per thread), then
-//               acc += chunk * (sa[kb][m] * sw[nb][kb]) in FP32 registers;
+//   warps 4..11 promotion: tcgen05.ld the chunk (one row per thread, 64
+//               columns per load), hand the TMEM buffer back as soon as the
+//               chunk is in registers, then acc += chunk * (sa[kb][m] *
+//               sw[nb][kb]) with packed FP32 FMAs (two columns per instruction);
 //               after the last chunk, BF16 (RNE) -> swizzled smem -> TMA store
 //               (dense) or row-masked coalesced stores (grouped)
 //
@@ -303,14 +305,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float row_mask = row_ok ? 1.0f : 0.0f;
       const int32_t col0 = n0 + half * kHalfCols;  // first column of this warp
       const float* sw_row = p.sw + (static_cast<int64_t>(group) * (p.N / 128) + col0 / 128) * p.KB;
-      float acc[kHalfCols];
+      // Pairs of FP32 accumulators, updated with packed FP32 FMAs.
+      float2 acc[kHalfCols / 2];
 #pragma unroll
-      for (int i = 0; i < kHalfCols; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < kHalfCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
       float sa_next = __ldg(sa_col);
       float sw_next = __ldg(sw_row);
       for (int kb = 0; kb < p.KB; ++kb) {
         const float scale = sa_next * sw_next * row_mask;
+        const float2 scale2 = make_float2(scale, scale);
         const int kn = kb + 1 < p.KB ? kb + 1 : kb;  // prefetch the next chunk's scales
         sa_next = __ldg(sa_col + static_cast<int64_t>(kn) * p.ld_sa);
         sw_next = __ldg(sw_row + kn);
@@ -323,15 +327,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + half * kHalfCols;
 #pragma unroll
-        for (int c = 0; c < kHalfCols / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_x32(taddr + c * 32, r);
-          tmem_wait_fma32(acc + c * 32, r, scale);
+        for (int c = 0; c < kHalfCols / 64; ++c) {
+          uint32_t r[64];
+          tmem_ld_x64(taddr + c * 64, r);
+          tmem_wait_ld(r);
+          if (c == kHalfCols / 64 - 1) {
+            // the whole chunk is in registers: hand the buffer back to the
+            // MMA warp before the last FMAs
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            acc[c * 32 + j] =
+                __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scale2,
+                           acc[c * 32 + j]);
         }
-        // whole chunk consumed: hand the buffer back to the MMA warp
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
         buf ^= 1u;
         if (buf == 0) bphase ^= 1u;
       }
@@ -346,11 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int c0 = piece * kEpiCols + j * 8;
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[c0 + 0], acc[c0 + 1]);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[c0 + 2], acc[c0 + 3]);
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[c0 + 4], acc[c0 + 5]);
-          __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[c0 + 6], acc[c0 + 7]);
+          const int c0 = (piece * kEpiCols + j * 8) / 2;
+          __nv_bfloat162 h0 = __float22bfloat162_rn(acc[c0 + 0]);
+          __nv_bfloat162 h1 = __float22bfloat162_rn(acc[c0 + 1]);
+          __nv_bfloat162 h2 = __float22bfloat162_rn(acc[c0 + 2]);
+          __nv_bfloat162 h3 = __float22bfloat162_rn(acc[c0 + 3]);
           uint4 v;
           v.x = *reinterpret_cast<uint32_t*>(&h0);
           v.y = *reinterpret_cast<uint32_t*>(&h1);

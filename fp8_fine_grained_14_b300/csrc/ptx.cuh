@@ -165,55 +165,24 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
          | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
 }
 
-// TMEM -> registers, 32 lanes x 32 consecutive 32-bit columns; thread i of the
+// TMEM -> registers, 32 lanes x 64 consecutive 32-bit columns; thread i of the
 // warp receives lane (base lane + i).  The registers are valid only after
-// tcgen05.wait::ld (see tmem_wait_fma32).
-__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+// tmem_wait_ld(r).
+__device__ __forceinline__ void tmem_ld_x64(uint32_t taddr, uint32_t (&r)[64]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr));
 }
 
-// Promotion step: wait for this warp's outstanding TMEM loads, then
-// acc[i] += chunk[i] * scale for 32 columns.  Wait and FMAs form one asm
-// statement: the loaded registers are read only after the wait, and each
-// chunk's FMAs stay between its load and the next one, which bounds the
-// number of live registers.
-__device__ __forceinline__ void tmem_wait_fma32(float* acc, const uint32_t (&r)[32], float scale) {
-  asm volatile(
-      "tcgen05.wait::ld.sync.aligned;\n\t"
-      "fma.rn.f32 %0, %32, %64, %0;\n\t fma.rn.f32 %1, %33, %64, %1;\n\t"
-      "fma.rn.f32 %2, %34, %64, %2;\n\t fma.rn.f32 %3, %35, %64, %3;\n\t"
-      "fma.rn.f32 %4, %36, %64, %4;\n\t fma.rn.f32 %5, %37, %64, %5;\n\t"
-      "fma.rn.f32 %6, %38, %64, %6;\n\t fma.rn.f32 %7, %39, %64, %7;\n\t"
-      "fma.rn.f32 %8, %40, %64, %8;\n\t fma.rn.f32 %9, %41, %64, %9;\n\t"
-      "fma.rn.f32 %10, %42, %64, %10;\n\t fma.rn.f32 %11, %43, %64, %11;\n\t"
-      "fma.rn.f32 %12, %44, %64, %12;\n\t fma.rn.f32 %13, %45, %64, %13;\n\t"
-      "fma.rn.f32 %14, %46, %64, %14;\n\t fma.rn.f32 %15, %47, %64, %15;\n\t"
-      "fma.rn.f32 %16, %48, %64, %16;\n\t fma.rn.f32 %17, %49, %64, %17;\n\t"
-      "fma.rn.f32 %18, %50, %64, %18;\n\t fma.rn.f32 %19, %51, %64, %19;\n\t"
-      "fma.rn.f32 %20, %52, %64, %20;\n\t fma.rn.f32 %21, %53, %64, %21;\n\t"
-      "fma.rn.f32 %22, %54, %64, %22;\n\t fma.rn.f32 %23, %55, %64, %23;\n\t"
-      "fma.rn.f32 %24, %56, %64, %24;\n\t fma.rn.f32 %25, %57, %64, %25;\n\t"
-      "fma.rn.f32 %26, %58, %64, %26;\n\t fma.rn.f32 %27, %59, %64, %27;\n\t"
-      "fma.rn.f32 %28, %60, %64, %28;\n\t fma.rn.f32 %29, %61, %64, %29;\n\t"
-      "fma.rn.f32 %30, %62, %64, %30;\n\t fma.rn.f32 %31, %63, %64, %31;"
-      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]), "+f"(acc[6]),
-        "+f"(acc[7]), "+f"(acc[8]), "+f"(acc[9]), "+f"(acc[10]), "+f"(acc[11]), "+f"(acc[12]), "+f"(acc[13]),
-        "+f"(acc[14]), "+f"(acc[15]), "+f"(acc[16]), "+f"(acc[17]), "+f"(acc[18]), "+f"(acc[19]), "+f"(acc[20]),
-        "+f"(acc[21]), "+f"(acc[22]), "+f"(acc[23]), "+f"(acc[24]), "+f"(acc[25]), "+f"(acc[26]), "+f"(acc[27]),
-        "+f"(acc[28]), "+f"(acc[29]), "+f"(acc[30]), "+f"(acc[31])
-      : "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
-        "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "f"(scale)
-      : "memory");
+// Wait for this thread's outstanding TMEM loads.  The loaded registers are
+// in/out operands, so no use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------

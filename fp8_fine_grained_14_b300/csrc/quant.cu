@@ -9,9 +9,10 @@
 //
 // Both kernels are HBM-bound (2 bytes read, 1 byte + 4/group written per
 // element): 16-byte vector loads, shuffle reductions, packed 8-byte code
-// stores.  Division is the correctly rounded __fdiv_rn (the build never
-// enables fast math or flush-to-zero), so codes and scales are bit-identical
-// to the float32 definition.
+// stores.  Scales use the correctly rounded __fdiv_rn; codes come from a
+// bracketing reciprocal product with an exact-division fallback (see
+// GroupScale).  The build never enables fast math or flush-to-zero, so codes
+// and scales are bit-identical to the float32 definition.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -22,16 +23,61 @@ namespace {
 
 constexpr float kE4M3Max = 448.0f;
 
-// Quantise 8 BF16 values (one 16-byte vector) with scale s into 8 codes.
-__device__ __forceinline__ uint2 quantise8(const uint4 v, float s) {
-  if (s == 0.0f) return make_uint2(0u, 0u);  // all-zero group
+// Per-group constants of the quantiser.
+//
+// The codes are defined as E4M3_RNE_satfinite(fl32(x / s)).  Dividing every
+// element is the slowest part of the kernel, so each element is first coded
+// from the two bracketing products x * r_lo and x * r_hi, with
+// r = fl32(1 / s) and r_lo / r_hi = r * (1 -/+ 2^-20) rounded.  Each product
+// rounds at most three times by 2^-24 relative, so the pair brackets the
+// correctly rounded quotient with a margin of more than 12 float32 ulps:
+// x * r_lo <= fl32(x / s) <= x * r_hi (order reversed for x < 0).  E4M3
+// rounding with saturation is monotonic, so when both ends give the same code
+// the quotient gives it too.  Only pairs whose bracket straddles a rounding
+// boundary (about 2^-16 of random data) fall back to the IEEE division.
+// Products that underflow keep the sign of x and code to +-0 on both ends,
+// as the quotient does.  Subnormal scales (1 / s would overflow) take the
+// division for the whole group.
+struct GroupScale {
+  float s;
+  float r_lo;
+  float r_hi;
+  bool bracket_ok;  // s is a normal float: the bracketing products are valid
+};
+
+__device__ __forceinline__ GroupScale group_scale(float amax) {
+  GroupScale g;
+  g.s = __fdiv_rn(amax, kE4M3Max);
+  g.bracket_ok = g.s >= 1.17549435e-38f;  // smallest normal float32
+  const float r = __frcp_rn(g.s);
+  g.r_lo = __fmul_rn(r, 1.0f - 0x1p-20f);
+  g.r_hi = __fmul_rn(r, 1.0f + 0x1p-20f);
+  return g;
+}
+
+// Codes of two values (a in the low byte) by correctly rounded division.
+__device__ __forceinline__ uint32_t quant_pair_div(float a, float b, float s) {
+  return cvt_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+}
+
+// Quantise 8 BF16 values (one 16-byte vector) of a group into 8 codes.
+__device__ __forceinline__ uint2 quantise8(const uint4 v, const GroupScale& g) {
+  if (g.s == 0.0f) return make_uint2(0u, 0u);  // all-zero group
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t pair[4];
+  bool same = true;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float lo = __fdiv_rn(bf16lo_to_f32(w[i]), s);
-    const float hi = __fdiv_rn(bf16hi_to_f32(w[i]), s);
-    pair[i] = cvt_e4m3x2(lo, hi);
+    const float a = bf16lo_to_f32(w[i]);
+    const float b = bf16hi_to_f32(w[i]);
+    const uint32_t lo = cvt_e4m3x2(__fmul_rn(a, g.r_lo), __fmul_rn(b, g.r_lo));
+    const uint32_t hi = cvt_e4m3x2(__fmul_rn(a, g.r_hi), __fmul_rn(b, g.r_hi));
+    pair[i] = lo;
+    same = same && (lo == hi);
+  }
+  if (!(same && g.bracket_ok)) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pair[i] = quant_pair_div(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), g.s);
   }
   return make_uint2(pair[0] | (pair[1] << 16), pair[2] | (pair[3] << 16));
 }
@@ -81,11 +127,11 @@ __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint4* __res
       float amax = absmax8(v[u]);
 #pragma unroll
       for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float s = __fdiv_rn(amax, kE4M3Max);
+      const GroupScale g = group_scale(amax);
       const int64_t kb = kb0 + u;
       if (row_ok && kb < KB) {
-        q[row * ldq_v + kb * 16 + lane16] = quantise8(v[u], s);
-        if (lane16 == 0) sa[kb * ld_sa + row] = s;
+        q[row * ldq_v + kb * 16 + lane16] = quantise8(v[u], g);
+        if (lane16 == 0) sa[kb * ld_sa + row] = g.s;
       }
     }
   }
@@ -96,7 +142,7 @@ __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint4* __res
 // column slice (t % 16) of rows (t / 16) + 16 i, i = 0..7, i.e. the whole
 // block sits in registers, so the block is read from HBM exactly once.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const uint4* __restrict__ w, int64_t NB,
+__global__ void __launch_bounds__(256, 3) quant_weight_128x128_kernel(const uint4* __restrict__ w, int64_t NB,
                                                                    int64_t KB, int64_t ldw_v, uint2* __restrict__ q,
                                                                    int64_t ldq_v, float* __restrict__ sw) {
   __shared__ float warp_max[8];
@@ -123,10 +169,10 @@ __global__ void __launch_bounds__(256) quant_weight_128x128_kernel(const uint4* 
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
     __syncthreads();  // warp_max is reused by the next block of this CTA
-    const float s = __fdiv_rn(amax, kE4M3Max);
-    if (threadIdx.x == 0) sw[nb * KB + kb] = s;
+    const GroupScale g = group_scale(amax);
+    if (threadIdx.x == 0) sw[nb * KB + kb] = g.s;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[(row0 + 16 * i) * ldq_v + kb * 16 + c] = quantise8(v[i], s);
+    for (int i = 0; i < 8; ++i) q[(row0 + 16 * i) * ldq_v + kb * 16 + c] = quantise8(v[i], g);
   }
 }
 

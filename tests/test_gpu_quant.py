@@ -107,6 +107,81 @@ def test_act_quant_strided_input_and_ld_sa():
     assert np.all(f32(sa)[:, 200:] == -1.0), "columns >= M of sa must be untouched"
 
 
+def inexact_scale_near_ties(seed=0):
+    """Groups whose quotients x / s sit a few float32 ulps off an E4M3
+    rounding boundary.
+
+    For amax with a short mantissa that is not a multiple of 7, s =
+    fl32(amax / 448) is inexact, while x = 21/16 * 2^e * amax / 448 (and
+    x = 7 * 2^-10 * amax / 448, a subnormal-range midpoint) is an exact BF16
+    value; x / s then lands within the scale's rounding error of the midpoint,
+    on the side that error decides.  These are the inputs on which a
+    reciprocal-multiply quantiser would disagree with the division."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for amax_m in range(33, 64, 2):
+        if amax_m % 7 == 0:
+            continue
+        for e0 in (-30, -7, 0, 9, 40):
+            amax = float(amax_m) * 2.0 ** (e0 - 5)
+            xs = [3.0 * amax * 2.0 ** (e - 10) for e in range(-6, 8)]  # m = 21/16 * 2^e
+            xs += [amax * 2.0 ** -16, 3.0 * amax * 2.0 ** -16]          # m = 7 * 2^-10, 21 * 2^-10
+            xs = np.array(xs, dtype=np.float64)
+            row = np.zeros(128, dtype=np.float32)
+            row[0] = amax
+            n = len(xs)
+            signs = np.where(rng.random(n) < 0.5, -1.0, 1.0)
+            row[1:1 + n] = (signs * xs).astype(np.float32)
+            row[1 + n:] = (rng.uniform(-1, 1, 127 - n) * amax).astype(np.float32)
+            rows.append(row)
+    x = np.stack(rows)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(f32(xb)[:, :17], x[:, :17]), "constructed values must be BF16-exact"
+    return xb
+
+
+def test_act_quant_near_ties_inexact_scale():
+    x = inexact_scale_near_ties()
+    _act_parity(x)
+    # the construction really produces quotients off a midpoint by less than 2^-20 relative
+    xf = f32(x).astype(np.float64)
+    s = oracle.fl32_div(np.max(np.abs(f32(x)), axis=1), np.float32(448.0)).astype(np.float64)
+    q = np.abs(xf[:, 1:15] / s[:, None])
+    e = np.floor(np.log2(q))
+    mant = q / 2.0 ** e  # in [1, 2)
+    assert np.all(np.abs(mant - 21 / 16) < 2.0 ** -20 * 21 / 16)
+
+
+def test_weight_quant_near_ties_inexact_scale():
+    rows = f32(inexact_scale_near_ties(seed=1))
+    # one 128x128 block per amax: the constructed row first, then rows well below amax
+    blocks = []
+    rng = np.random.default_rng(2)
+    for r in rows[:12]:
+        blk = (rng.uniform(-0.5, 0.5, (128, 128)) * float(np.max(np.abs(r)))).astype(np.float32)
+        blk[0] = r
+        blocks.append(blk)
+    w = torch.from_numpy(np.concatenate(blocks, axis=0)).to(torch.bfloat16)
+    _weight_parity(w)
+
+
+@pytest.mark.parametrize("M,K", [(4096, 4096)])
+def test_act_quant_random_sweep(M, K):
+    """16.7M elements with a random power-of-two magnitude per row: every code
+    and scale matches the oracle (exercises both the bracketing fast path
+    and its division fallback on near-boundary quotients)."""
+    g = torch.Generator().manual_seed(123)
+    x = torch.randn(M, K, generator=g) * torch.pow(2.0, torch.randint(-40, 40, (M, 1), generator=g).float())
+    _act_parity(x.to(torch.bfloat16))
+
+
+def test_weight_quant_random_sweep():
+    g = torch.Generator().manual_seed(321)
+    w = torch.randn(4096, 4096, generator=g)
+    w = w * torch.pow(2.0, torch.randint(-40, 40, (32, 1, 32, 1), generator=g).float()).expand(32, 128, 32, 128).reshape(4096, 4096)
+    _weight_parity(w.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("name", ["up", "down", "decode"])
 def test_quant_full_size_sampled(name):
     """Full-size configurations, launched as the benchmark launches them;
