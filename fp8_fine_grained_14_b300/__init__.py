@@ -13,10 +13,12 @@ _API = (
     "fp8_quant_weight_128x128",
     "fp8_blockscaled_gemm",
     "fp8_blockscaled_grouped_gemm",
+    "fp8_dequant_weight_128x128",
     "fp8bs_last_device_error",
     "fp8bs_set_wait_timeout_ns",
     "fp8bs_selftest_wait_timeout",
     "linear_forward",
+    "HostPipeline",
     "ld_sa_for",
     "Fp8bsError",
 )

@@ -32,6 +32,9 @@ EXPORTS = {
     "fp8_quant_weight_128x128": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
     "fp8_blockscaled_gemm": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_grouped_gemm": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
+    "fp8_blockscaled_gemm_f32": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
+    "fp8_blockscaled_grouped_gemm_f32": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
+    "fp8_dequant_weight_128x128": [_p, _i64, _i64, _i64, _p, _p, _i64, _p],
     "fp8bs_status_string": [ctypes.c_int],
     "fp8bs_last_error_detail": [],
     "fp8bs_last_device_error": [_p],
@@ -125,29 +128,35 @@ def fp8_quant_weight_128x128(w, qw=None, sw=None, stream=None):
     return qw, sw
 
 
-def fp8_blockscaled_gemm(qa, sa, qw, sw, y=None, stream=None):
-    """Block-scaled FP8 GEMM: Y bf16 [M, N] from qa [M, K], sa [K/128, ld_sa],
-    qw [N, K], sw [N/128, K/128]."""
+def fp8_blockscaled_gemm(qa, sa, qw, sw, y=None, stream=None, out_dtype=torch.bfloat16):
+    """Block-scaled FP8 GEMM: Y [M, N] from qa [M, K], sa [K/128, ld_sa],
+    qw [N, K], sw [N/128, K/128].  Y is BF16 (fp8_blockscaled_gemm) or FP32
+    (fp8_blockscaled_gemm_f32), following `y`'s dtype when y is given."""
     _require(qa, torch.uint8, "qa", 2)
     _require(qw, torch.uint8, "qw", 2)
     _require(sa, torch.float32, "sa", 2)
     M, K = qa.shape
     N = qw.shape[0]
     if y is None:
-        y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    _require(y, torch.bfloat16, "y", 2)
+        y = torch.empty((M, N), dtype=out_dtype, device=qa.device)
+    if y.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("y must be bfloat16 or float32")
+    _require(y, y.dtype, "y", 2)
     if not sw.is_contiguous():
         raise ValueError("sw must be contiguous")
-    st = lib.fp8_blockscaled_gemm(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
-                                  _ptr(y), y.stride(0), M, N, K, _stream(stream))
-    _check("fp8_blockscaled_gemm", st)
+    fn = "fp8_blockscaled_gemm" if y.dtype == torch.bfloat16 else "fp8_blockscaled_gemm_f32"
+    st = getattr(lib, fn)(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
+                          _ptr(y), y.stride(0), M, N, K, _stream(stream))
+    _check(fn, st)
     return y
 
 
-def fp8_blockscaled_grouped_gemm(group_offsets, m_total, qa, sa, qw, sw, y=None, stream=None):
+def fp8_blockscaled_grouped_gemm(group_offsets, m_total, qa, sa, qw, sw, y=None, stream=None,
+                                 out_dtype=torch.bfloat16):
     """Grouped GEMM: rows off[g]..off[g+1]-1 use expert g's weights.
     group_offsets: CUDA int32 [G+1]; m_total: host int equal to off[G];
-    qw uint8 [G, N, K]; sw float32 [G, N/128, K/128]."""
+    qw uint8 [G, N, K]; sw float32 [G, N/128, K/128].  Y is BF16 or FP32
+    (following `y`'s dtype when given)."""
     if group_offsets.dtype != torch.int32 or not group_offsets.is_cuda or not group_offsets.is_contiguous():
         raise TypeError("group_offsets must be a contiguous CUDA int32 tensor")
     _require(qa, torch.uint8, "qa", 2)
@@ -156,12 +165,35 @@ def fp8_blockscaled_grouped_gemm(group_offsets, m_total, qa, sa, qw, sw, y=None,
         raise ValueError("qw [G, N, K] and sw [G, N/128, K/128] must be contiguous")
     G, N, K = qw.shape
     if y is None:
-        y = torch.empty((m_total, N), dtype=torch.bfloat16, device=qa.device)
+        y = torch.empty((m_total, N), dtype=out_dtype, device=qa.device)
+    if y.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("y must be bfloat16 or float32")
+    _require(y, y.dtype, "y", 2)
+    fn = "fp8_blockscaled_grouped_gemm" if y.dtype == torch.bfloat16 else "fp8_blockscaled_grouped_gemm_f32"
+    st = getattr(lib, fn)(G, _ptr(group_offsets), int(m_total), _ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0),
+                          _ptr(qw), _ptr(sw), _ptr(y), y.stride(0), N, K, _stream(stream))
+    _check(fn, st)
+    return y
+
+
+def fp8_dequant_weight_128x128(qw, sw, y=None, stream=None):
+    """qw uint8 [N, K] (or [G, N, K]) + sw float32 [N/128, K/128] (or
+    [G, N/128, K/128]) -> BF16 weights of the same shape."""
+    if qw.dim() == 3:
+        G, N, K = qw.shape
+        y3 = y if y is not None else torch.empty((G, N, K), dtype=torch.bfloat16, device=qw.device)
+        fp8_dequant_weight_128x128(qw.reshape(G * N, K), sw.reshape(G * N // 128, K // 128), y3.view(G * N, K),
+                                   stream=stream)
+        return y3
+    _require(qw, torch.uint8, "qw", 2)
+    N, K = qw.shape
+    if y is None:
+        y = torch.empty((N, K), dtype=torch.bfloat16, device=qw.device)
     _require(y, torch.bfloat16, "y", 2)
-    st = lib.fp8_blockscaled_grouped_gemm(G, _ptr(group_offsets), int(m_total), _ptr(qa), qa.stride(0), _ptr(sa),
-                                          sa.stride(0), _ptr(qw), _ptr(sw), _ptr(y), y.stride(0), N, K,
-                                          _stream(stream))
-    _check("fp8_blockscaled_grouped_gemm", st)
+    if not sw.is_contiguous() or sw.dtype != torch.float32:
+        raise ValueError("sw must be a contiguous float32 tensor")
+    st = lib.fp8_dequant_weight_128x128(_ptr(qw), N, K, qw.stride(0), _ptr(sw), _ptr(y), y.stride(0), _stream(stream))
+    _check("fp8_dequant_weight_128x128", st)
     return y
 
 
@@ -176,6 +208,79 @@ def fp8bs_set_wait_timeout_ns(ns: int):
 
 def fp8bs_selftest_wait_timeout(ns: int, stream=None):
     _check("fp8bs_selftest_wait_timeout", lib.fp8bs_selftest_wait_timeout(int(ns), _stream(stream)))
+
+
+class HostPipeline:
+    """The whole hot path on batches held in (pinned) host memory.
+
+    Each submit() copies one batch (X, and W unless it is quantised once up
+    front) host -> device, runs 1x128 activation quantisation, 128x128 weight
+    quantisation and the block-scaled GEMM, and copies Y device -> host.  The
+    three phases use three CUDA streams and `depth` sets of device buffers, so
+    the copies of one batch overlap the kernels and copies of its neighbours.
+    All arithmetic runs in the library's kernels; this class only owns
+    buffers, streams and events.
+
+    prequantised_w: a (qw, sw) pair already on the device (decode-style
+    serving, where the weights stay resident); then only X moves per batch.
+    """
+
+    def __init__(self, M, N, K, device="cuda", depth=2, prequantised_w=None):
+        dev = torch.device(device)
+        self.M, self.N, self.K, self.depth = M, N, K, depth
+        self.h2d = torch.cuda.Stream(dev)
+        self.compute = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.fixed_w = prequantised_w
+        self.slots = []
+        for _ in range(depth):
+            slot = {
+                "x": torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                "qa": torch.empty((M, K), dtype=torch.uint8, device=dev),
+                "sa": torch.empty((K // 128, ld_sa_for(M)), dtype=torch.float32, device=dev),
+                "y": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                "loaded": torch.cuda.Event(), "computed": torch.cuda.Event(), "stored": torch.cuda.Event(),
+                "used": False,
+            }
+            if prequantised_w is None:
+                slot["w"] = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+                slot["qw"] = torch.empty((N, K), dtype=torch.uint8, device=dev)
+                slot["sw"] = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+            self.slots.append(slot)
+        self.next = 0
+
+    def submit(self, x_host, w_host, y_host):
+        """Queue one batch; returns the event that completes when y_host holds Y."""
+        slot = self.slots[self.next]
+        self.next = (self.next + 1) % self.depth
+        if slot["used"]:
+            self.h2d.wait_event(slot["computed"])   # inputs of the slot's previous batch consumed
+        with torch.cuda.stream(self.h2d):
+            slot["x"].copy_(x_host, non_blocking=True)
+            if self.fixed_w is None:
+                slot["w"].copy_(w_host, non_blocking=True)
+            slot["loaded"].record(self.h2d)
+        self.compute.wait_event(slot["loaded"])
+        if slot["used"]:
+            self.compute.wait_event(slot["stored"])  # previous Y of the slot copied out
+        fp8_quant_act_1x128(slot["x"], qa=slot["qa"], sa=slot["sa"], stream=self.compute)
+        if self.fixed_w is None:
+            fp8_quant_weight_128x128(slot["w"], qw=slot["qw"], sw=slot["sw"], stream=self.compute)
+            qw, sw = slot["qw"], slot["sw"]
+        else:
+            qw, sw = self.fixed_w
+        fp8_blockscaled_gemm(slot["qa"], slot["sa"], qw, sw, y=slot["y"], stream=self.compute)
+        slot["computed"].record(self.compute)
+        self.d2h.wait_event(slot["computed"])
+        with torch.cuda.stream(self.d2h):
+            y_host.copy_(slot["y"], non_blocking=True)
+            slot["stored"].record(self.d2h)
+        slot["used"] = True
+        return slot["stored"]
+
+    def synchronize(self):
+        for st in (self.h2d, self.compute, self.d2h):
+            st.synchronize()
 
 
 def linear_forward(x, w, stream=None):

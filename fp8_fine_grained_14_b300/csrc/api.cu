@@ -186,30 +186,35 @@ fp8bs_status fp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, 
   return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_weight_128x128 launch", e);
 }
 
-fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,
-                                  int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,
-                                  int64_t K, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared validation and launch of the dense GEMM; out_bytes is 2 (BF16 y) or
+// 4 (FP32 y) and sets the row-stride rule for y.
+fp8bs_status dense_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw, int64_t ldqw,
+                        const float* sw, void* y, int64_t ldy, int out_bytes, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream, const char* name) {
   if (M < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldqw < 0 || ldy < 0) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim)
     return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (ldqa < K || ldqw < K || ldy < N || ld_sa < M) return FP8BS_ERR_INVALID_ARG;
   if (M == 0) return FP8BS_OK;
-  if (qa == nullptr || sa == nullptr || qw == nullptr || sw == nullptr || y_bf16 == nullptr)
-    return FP8BS_ERR_INVALID_ARG;
-  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qw) || !aligned16(sw) || !aligned16(y_bf16) ||
-      ldqa % 16 != 0 || ldqw % 16 != 0 || ldy % 8 != 0 || ld_sa % 4 != 0)
+  if (qa == nullptr || sa == nullptr || qw == nullptr || sw == nullptr || y == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qw) || !aligned16(sw) || !aligned16(y) || ldqa % 16 != 0 ||
+      ldqw % 16 != 0 || (ldy * out_bytes) % 16 != 0 || ld_sa % 4 != 0)
     return FP8BS_ERR_MISALIGNED;
   cudaError_t e;
   const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
   if (dev == nullptr) return cuda_failure("device query", e);
-  e = fp8bs::launch_blockscaled_gemm(*dev, qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, M, N, K, stream);
-  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_blockscaled_gemm launch", e);
+  e = fp8bs::launch_blockscaled_gemm(*dev, qa, ldqa, sa, ld_sa, qw, ldqw, sw, y, ldy, out_bytes == 4, M, N, K,
+                                     stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure(name, e);
 }
 
-fp8bs_status fp8_blockscaled_grouped_gemm(int32_t G, const int32_t* group_offsets_dev, int64_t M_total,
-                                          const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
-                                          const void* qw, const float* sw, void* y_bf16, int64_t ldy, int64_t N,
-                                          int64_t K, cudaStream_t stream) {
+fp8bs_status grouped_gemm(int32_t G, const int32_t* group_offsets_dev, int64_t M_total, const void* qa, int64_t ldqa,
+                          const float* sa, int64_t ld_sa, const void* qw, const float* sw, void* y, int64_t ldy,
+                          int out_bytes, int64_t N, int64_t K, cudaStream_t stream, const char* name) {
   if (G <= 0 || G > 65536 || M_total < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldy < 0)
     return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || M_total > kMaxDim ||
@@ -218,18 +223,67 @@ fp8bs_status fp8_blockscaled_grouped_gemm(int32_t G, const int32_t* group_offset
   if (ldqa < K || ldy < N || ld_sa < M_total) return FP8BS_ERR_INVALID_ARG;
   if (group_offsets_dev == nullptr) return FP8BS_ERR_INVALID_ARG;
   if (M_total == 0) return FP8BS_OK;
-  if (qa == nullptr || sa == nullptr || qw == nullptr || sw == nullptr || y_bf16 == nullptr)
-    return FP8BS_ERR_INVALID_ARG;
-  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qw) || !aligned16(sw) || !aligned16(y_bf16) ||
-      (reinterpret_cast<uintptr_t>(group_offsets_dev) & 3u) != 0 || ldqa % 16 != 0 || ldy % 8 != 0 ||
+  if (qa == nullptr || sa == nullptr || qw == nullptr || sw == nullptr || y == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qw) || !aligned16(sw) || !aligned16(y) ||
+      (reinterpret_cast<uintptr_t>(group_offsets_dev) & 3u) != 0 || ldqa % 16 != 0 || (ldy * out_bytes) % 16 != 0 ||
       ld_sa % 4 != 0)
     return FP8BS_ERR_MISALIGNED;
   cudaError_t e;
   const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
   if (dev == nullptr) return cuda_failure("device query", e);
-  e = fp8bs::launch_blockscaled_grouped_gemm(*dev, G, group_offsets_dev, M_total, qa, ldqa, sa, ld_sa, qw, sw,
-                                             y_bf16, ldy, N, K, stream);
-  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_blockscaled_grouped_gemm launch", e);
+  e = fp8bs::launch_blockscaled_grouped_gemm(*dev, G, group_offsets_dev, M_total, qa, ldqa, sa, ld_sa, qw, sw, y,
+                                             ldy, out_bytes == 4, N, K, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure(name, e);
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,
+                                  int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,
+                                  int64_t K, cudaStream_t stream) {
+  return dense_gemm(qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, 2, M, N, K, stream, "fp8_blockscaled_gemm launch");
+}
+
+fp8bs_status fp8_blockscaled_gemm_f32(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,
+                                      int64_t ldqw, const float* sw, float* y_f32, int64_t ldy, int64_t M, int64_t N,
+                                      int64_t K, cudaStream_t stream) {
+  return dense_gemm(qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_f32, ldy, 4, M, N, K, stream,
+                    "fp8_blockscaled_gemm_f32 launch");
+}
+
+fp8bs_status fp8_blockscaled_grouped_gemm(int32_t G, const int32_t* group_offsets_dev, int64_t M_total,
+                                          const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                          const void* qw, const float* sw, void* y_bf16, int64_t ldy, int64_t N,
+                                          int64_t K, cudaStream_t stream) {
+  return grouped_gemm(G, group_offsets_dev, M_total, qa, ldqa, sa, ld_sa, qw, sw, y_bf16, ldy, 2, N, K, stream,
+                      "fp8_blockscaled_grouped_gemm launch");
+}
+
+fp8bs_status fp8_blockscaled_grouped_gemm_f32(int32_t G, const int32_t* group_offsets_dev, int64_t M_total,
+                                              const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                              const void* qw, const float* sw, float* y_f32, int64_t ldy, int64_t N,
+                                              int64_t K, cudaStream_t stream) {
+  return grouped_gemm(G, group_offsets_dev, M_total, qa, ldqa, sa, ld_sa, qw, sw, y_f32, ldy, 4, N, K, stream,
+                      "fp8_blockscaled_grouped_gemm_f32 launch");
+}
+
+fp8bs_status fp8_dequant_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, const float* sw,
+                                        void* y_bf16, int64_t ldy, cudaStream_t stream) {
+  if (N < 0 || K < 0 || ldq < 0 || ldy < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldq < K || ldy < K) return FP8BS_ERR_INVALID_ARG;
+  if (qw == nullptr || sw == nullptr || y_bf16 == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qw) || !aligned16(y_bf16) || (reinterpret_cast<uintptr_t>(sw) & 3u) != 0 || ldq % 16 != 0 ||
+      ldy % 8 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_dequant_weight_128x128(*dev, qw, N, K, ldq, sw, y_bf16, ldy, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_dequant_weight_128x128 launch", e);
 }
 
 fp8bs_status fp8bs_last_device_error(cudaStream_t stream) {

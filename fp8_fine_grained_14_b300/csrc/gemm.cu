@@ -8,8 +8,9 @@
 // H800 alternates two warpgroups between WGMMA and promotion).  On sm_103a
 // the same overlap comes from two TMEM accumulator buffers:
 //
-//   warp 0      TMA producer: A (128x128 codes) and B (BNx128 codes) per K
-//               chunk into a STAGES-deep shared-memory ring (mbarrier full/empty)
+//   warp 0      TMA producer: A (128x128 codes) and B (BN/CG x 128 codes) per
+//               K chunk into a STAGES-deep shared-memory ring (mbarrier
+//               full/empty)
 //   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma kind::f8f6f4
 //               (K = 32 each) per chunk into TMEM buffer (chunk & 1), then
 //               tcgen05.commit to free the smem stage and publish the chunk
@@ -21,16 +22,27 @@
 //               after the last chunk, BF16 (RNE) -> swizzled smem -> TMA store
 //               (dense) or row-masked coalesced stores (grouped)
 //
-// While the promotion warps drain buffer b, the MMA warp fills buffer b^1.
-// The kernel is persistent: CTA i handles tiles i, i + grid, ...; tiles are
-// ordered M-fastest so a wave of CTAs shares a few weight column blocks
+// Wide tiles run on CTA pairs (CG = 2, a cluster of two CTAs on two SMs):
+// the pair computes a 256 x 256 tile with tcgen05 cta_group::2 MMAs issued by
+// the even CTA.  Each CTA holds its 128 rows of A and half (128 columns) of B
+// per stage, so a stage is 32 KB and six stages fit beside the epilogue
+// staging: deep enough to cover the L2 latency of the operand loads at the
+// tensor pipe's rate.  Each CTA's TMEM holds its 128 rows of the accumulator,
+// and each CTA promotes and stores its own rows.  Narrow tiles (BN = 128, for
+// skinny M) run on single CTAs (CG = 1).
+//
+// The kernel is persistent: cluster c handles tiles c, c + clusters, ...;
+// tiles are ordered M-fastest so a wave shares a few weight column blocks
 // (L2-resident) and the whole activation matrix.
 //
 // Every mbarrier wait is bounded (see ptx.cuh).  A wait that gives up records
 // a timeout in the status word and raises a CTA-wide abort flag; every role
 // then leaves its loop, the producer drains its TMA loads, the MMA warp waits
-// for its last commits, and TMEM is released before the CTA exits.
+// for its last commits, and TMEM is released before the CTA exits.  The peer
+// of an aborting CTA stops on its own bounded waits.
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -45,7 +57,7 @@ constexpr int kThreads = 384;         // 12 warps = 3 warpgroups
 constexpr int kEpiWarps = 8;          // warps 4..11
 constexpr int kFirstEpiWarp = 4;
 constexpr int kStagingBytes = 4096;   // per promotion warp: 32 rows x 64 BF16
-constexpr int kEpiCols = 64;          // columns per TMA store box
+constexpr int kEpiRowBytes = 128;     // bytes of one staged output row (one 128B-swizzle row)
 // Register split for 256-wide tiles (setmaxnreg): warpgroup 0 (TMA, MMA,
 // idle) drops to RegSplit::low, the two promotion warpgroups rise to
 // RegSplit::high.  Every SM sub-partition hosts one warp of each warpgroup, so
@@ -65,7 +77,7 @@ struct Params {
   const float* sa;
   int64_t ld_sa;
   const float* sw;
-  __nv_bfloat16* y;     // grouped: direct stores
+  void* y;              // grouped: direct stores (BF16 or FP32)
   int64_t ldy;
   int32_t M;            // rows of A (M_total when grouped)
   int32_t N;
@@ -76,10 +88,10 @@ struct Params {
   uint64_t timeout_ns;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 struct Smem {
   static constexpr int kA = BM * BK;
-  static constexpr int kB = BN * BK;
+  static constexpr int kB = (BN / CG) * BK;  // this CTA's share of the B tile
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kA;
   static constexpr int kOffStaging = kOffB + STAGES * kB;
@@ -91,20 +103,29 @@ struct Smem {
   static constexpr int kDynamic = kBytes + 1024;  // + alignment slack
 };
 
-// Tile walker shared by all roles: yields (a_row, row_end, b_row, n0, group)
-// for this CTA's tiles in order.  Dense: one group of M rows.  Grouped:
-// group g has rows off[g] .. off[g+1]-1 and weight rows g*N .. g*N+N-1.
-template <bool GROUPED, int BN>
+// Tile walker shared by all roles.  Tiles are visited in "cluster tiles" of
+// CM consecutive 128-row tiles x one BN-column tile; the CM CTAs of a
+// cluster walk the same cluster tiles in the same order and CTA `rank` takes
+// row tile CM * m + rank of each.  Yields (a_row, row_end, b_row, n0, group)
+// per tile; b_row is the first weight row of the whole BN-column tile.  A row
+// tile may lie wholly past row_end (an odd count of row tiles): its CTA still
+// loads and takes part in the pair's MMAs, and its outputs are masked.  Dense: one group of M rows.  Grouped: group g has rows
+// off[g] .. off[g+1]-1 and weight rows g*N .. g*N+N-1.
+template <bool GROUPED, int BN, int CM>
 struct TileWalker {
   const Params& p;
-  int64_t next;        // next global tile index for this CTA
-  int32_t n_tiles;     // N / BN
+  int64_t next;          // next cluster tile of this cluster
+  int64_t stride;        // clusters in the grid
+  int32_t rank;          // this CTA's rank in its cluster
+  int32_t n_tiles;       // N / BN
   // grouped state
   int32_t g;
-  int64_t tiles_before;  // tiles of groups < g
-  int32_t g_row0, g_row1, g_mtiles;
+  int64_t tiles_before;  // cluster tiles of groups < g
+  int32_t g_row0, g_row1, g_mgroups;
 
-  __device__ TileWalker(const Params& p_) : p(p_), next(blockIdx.x), n_tiles(p_.N / BN), g(0), tiles_before(0) {
+  __device__ TileWalker(const Params& p_, int32_t rank_)
+      : p(p_), next(blockIdx.x / CM), stride(gridDim.x / CM), rank(rank_), n_tiles(p_.N / BN), g(0),
+        tiles_before(0) {
     if (GROUPED) load_group();
   }
   __device__ void load_group() {
@@ -116,34 +137,34 @@ struct TileWalker {
     }
     g_row0 = r0;
     g_row1 = r1;
-    g_mtiles = (r1 - r0 + BM - 1) / BM;
+    g_mgroups = ((r1 - r0 + BM - 1) / BM + CM - 1) / CM;
   }
   // Returns false when this CTA has no more tiles.
   __device__ bool get(int32_t& a_row, int32_t& row_end, int32_t& b_row, int32_t& n0, int32_t& group) {
     const int64_t t = next;
-    next += gridDim.x;
+    next += stride;
     if (!GROUPED) {
-      const int32_t m_tiles = (p.M + BM - 1) / BM;
-      if (t >= static_cast<int64_t>(m_tiles) * n_tiles) return false;
-      const int32_t mt = static_cast<int32_t>(t % m_tiles);
-      const int32_t nt = static_cast<int32_t>(t / m_tiles);
-      a_row = mt * BM;
+      const int32_t m_groups = ((p.M + BM - 1) / BM + CM - 1) / CM;
+      if (t >= static_cast<int64_t>(m_groups) * n_tiles) return false;
+      const int32_t mg = static_cast<int32_t>(t % m_groups);
+      const int32_t nt = static_cast<int32_t>(t / m_groups);
+      a_row = (mg * CM + rank) * BM;
       row_end = p.M;
       n0 = nt * BN;
       b_row = n0;
       group = 0;
       return true;
     } else {
-      while (g < p.G && t >= tiles_before + static_cast<int64_t>(g_mtiles) * n_tiles) {
-        tiles_before += static_cast<int64_t>(g_mtiles) * n_tiles;
+      while (g < p.G && t >= tiles_before + static_cast<int64_t>(g_mgroups) * n_tiles) {
+        tiles_before += static_cast<int64_t>(g_mgroups) * n_tiles;
         ++g;
         load_group();
       }
       if (g >= p.G) return false;
       const int64_t local = t - tiles_before;
-      const int32_t mt = static_cast<int32_t>(local % g_mtiles);
-      const int32_t nt = static_cast<int32_t>(local / g_mtiles);
-      a_row = g_row0 + mt * BM;
+      const int32_t mg = static_cast<int32_t>(local % g_mgroups);
+      const int32_t nt = static_cast<int32_t>(local / g_mgroups);
+      a_row = g_row0 + (mg * CM + rank) * BM;
       row_end = g_row1;
       n0 = nt * BN;
       b_row = g * p.N + n0;
@@ -158,17 +179,21 @@ __device__ __forceinline__ void abort_cta(volatile int* abort_flag, unsigned* st
   record_status(status, kStatusTimeout);
 }
 
-template <int BN, int STAGES, bool GROUPED>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32>
 __global__ void __launch_bounds__(kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using L = Smem<BN, STAGES>;
-  constexpr int kTmemCols = 2 * BN;   // two accumulator buffers
+  using L = Smem<BN, STAGES, CG>;
+  static_assert(CG == 1 || CG == 2, "single CTAs or CTA pairs");
+  constexpr int kTmemCols = 2 * BN;   // two accumulator buffers of this CTA's 128 rows x BN
   constexpr int kHalfCols = BN / 2;   // columns per promotion warp
-  constexpr uint32_t kStageTx = L::kA + L::kB;
-  constexpr uint32_t kIdesc = idesc_e4m3_f32(BM, BN);
+  constexpr uint32_t kStageTx = CG * (L::kA + L::kB);  // bytes landing per stage (whole pair)
+  constexpr uint32_t kIdesc = idesc_e4m3_f32(BM * CG, BN);
+  constexpr uint16_t kPairMask = 0x3;
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of two");
-  static_assert(kHalfCols % kEpiCols == 0, "epilogue boxes");
+  constexpr int kOutBytes = F32 ? 4 : 2;
+  constexpr int kPieceCols = kEpiRowBytes / kOutBytes;  // output columns per staged piece
+  static_assert(kHalfCols % kPieceCols == 0, "epilogue boxes");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -184,15 +209,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int32_t rank = CG > 1 ? static_cast<int32_t>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;  // issues the pair's MMAs and owns its full / tempty barriers
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_full + 8 * s, 1);   // the leader's producer arrives; all loads of the pair credit bytes
+      mbar_init(bar_empty + 8 * s, 1);  // released by the (leader's) MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, kEpiWarps);
+      mbar_init(bar_tempty + 8 * b, kEpiWarps * CG);  // every promotion warp of the pair
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -201,15 +228,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!GROUPED) prefetch_tmap(&tmY);
   }
   if (warp == 1) {
-    tmem_alloc(base + L::kOffSlot, kTmemCols);
-    tmem_relinquish();
+    if (CG == 1) {
+      tmem_alloc(base + L::kOffSlot, kTmemCols);
+      tmem_relinquish();
+    } else {
+      tmem_alloc_pair(base + L::kOffSlot, kTmemCols);
+      tmem_relinquish_pair();
+    }
   }
+  // Barriers and TMEM must be ready in both CTAs of a pair before either
+  // signals the other.
   tc_fence_before_sync();
-  __syncthreads();
+  if (CG > 1)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // The pair's full and tempty barriers live in the leader.
+  const uint32_t full_base = CG > 1 ? map_shared_rank(bar_full, 0) : bar_full;
+  const uint32_t tempty_base = CG > 1 ? map_shared_rank(bar_tempty, 0) : bar_tempty;
 
-  TileWalker<GROUPED, BN> tiles(p);
+  TileWalker<GROUPED, BN, CG> tiles(p, rank);
   int32_t a_row, row_end, b_row, n0, group;
 
   if (warp < kFirstEpiWarp) {
@@ -217,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // launch allocation: this warpgroup hands registers to the other two.
     if (BN == 256) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(RegSplit<GROUPED>::low));
     if (warp == 0 && lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs of a pair) ----------------
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;  // per stage: ever issued / parity of last issue
       bool ok = true;
@@ -228,10 +268,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t full = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(full, kStageTx);
-          tma_load_2d(base + L::kOffA + stage * L::kA, &tmA, full, kb * BK, a_row);
-          tma_load_2d(base + L::kOffB + stage * L::kB, &tmB, full, kb * BK, b_row);
+          const uint32_t a_dst = base + L::kOffA + stage * L::kA;
+          const uint32_t b_dst = base + L::kOffB + stage * L::kB;
+          if (CG == 1) {
+            const uint32_t full = bar_full + 8 * stage;
+            mbar_arrive_expect_tx(full, kStageTx);
+            tma_load_2d(a_dst, &tmA, full, kb * BK, a_row);
+            tma_load_2d(b_dst, &tmB, full, kb * BK, b_row);
+          } else {
+            // the leader expects the whole pair's bytes; each CTA loads its
+            // own A rows and its half of B and credits the leader's barrier
+            if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, kStageTx);
+            const uint32_t full = full_base + 8 * stage;
+            tma_load_2d_pair(a_dst, &tmA, full, kb * BK, a_row);
+            tma_load_2d_pair(b_dst, &tmB, full, kb * BK, b_row + rank * (BN / CG));
+          }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -241,20 +292,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        // Let every load already issued land before shared memory goes away.
+        // Let every load already issued land before shared memory goes away
+        // (the pair's loads are counted on the leader's barriers).
+        if (leader)
+          for (int s = 0; s < STAGES; ++s)
+            if (issued_mask & (1u << s))
+              (void)mbar_wait(bar_full + 8 * s, (issued_parity >> s) & 1u, nullptr, p.timeout_ns);
+      } else {
+        // Wait for the last release of every stage, so that no MMA still
+        // reads this CTA's shared memory and no commit still targets it.
         for (int s = 0; s < STAGES; ++s)
           if (issued_mask & (1u << s))
-            (void)mbar_wait(bar_full + 8 * s, (issued_parity >> s) & 1u, nullptr, p.timeout_ns);
+            (void)mbar_wait(bar_empty + 8 * s, (issued_parity >> s) & 1u, abort_flag, p.timeout_ns);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------- MMA issuer ----------------
+    } else if (warp == 1 && lane == 0 && leader) {
+      // ---------------- MMA issuer (the leader of a pair) ----------------
       uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
       uint32_t committed = 0, committed_parity = 0;  // per TMEM buffer: ever committed / parity of last commit
       bool ok = true;
       while (ok && tiles.get(a_row, row_end, b_row, n0, group)) {
         for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag, p.timeout_ns) ||
-              !mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.timeout_ns)) {
+          // (with a pair, the peer's promotion warps also release the buffer)
+          const bool drained = CG == 1 ? mbar_wait(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag, p.timeout_ns)
+                                       : mbar_wait_cluster(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag,
+                                                           p.timeout_ns);
+          if (!drained || !mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.timeout_ns)) {
             abort_cta(abort_flag, p.status);
             ok = false;
             break;
@@ -266,10 +328,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / MMA_K; ++k) {
             // advance the start address by 32 bytes (2 units of 16 B) per K step
-            mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
+            if (CG == 1)
+              mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
+            else
+              mma_f8f6f4_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
           }
-          mma_commit(bar_empty + 8 * stage);  // smem stage reusable once these MMAs finish
-          mma_commit(bar_tfull + 8 * buf);    // chunk kb ready in TMEM buffer `buf`
+          if (CG == 1) {
+            mma_commit(bar_empty + 8 * stage);  // smem stage reusable once these MMAs finish
+            mma_commit(bar_tfull + 8 * buf);    // chunk kb ready in TMEM buffer `buf`
+          } else {
+            mma_commit_pair(bar_empty + 8 * stage, kPairMask);  // both CTAs' stages
+            mma_commit_pair(bar_tfull + 8 * buf, kPairMask);    // both CTAs' accumulator rows
+          }
           committed |= 1u << buf;
           committed_parity = (committed_parity & ~(1u << buf)) | (bphase << buf);
           if (++stage == STAGES) {
@@ -300,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && tiles.get(a_row, row_end, b_row, n0, group)) {
       const int32_t row = a_row + q * 32 + lane;  // this thread's output row
       const bool row_ok = row < row_end;
-      // rows past the end read a valid row's scale (no divergent loads) and drop it
-      const float* sa_col = p.sa + (row_ok ? row : a_row);
+      // rows past the end read a valid row's scale and drop the result
+      const float* sa_col = p.sa + min(row, p.M - 1);
       const float row_mask = row_ok ? 1.0f : 0.0f;
       const int32_t col0 = n0 + half * kHalfCols;  // first column of this warp
       const float* sw_row = p.sw + (static_cast<int64_t>(group) * (p.N / 128) + col0 / 128) * p.KB;
@@ -333,10 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld(r);
           if (c == kHalfCols / 64 - 1) {
             // the whole chunk is in registers: hand the buffer back to the
-            // MMA warp before the last FMAs
+            // MMA warp (of the pair's leader) before the last FMAs
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+            if (lane == 0) {
+              if (CG == 1)
+                mbar_arrive_relaxed(bar_tempty + 8 * buf);
+              else
+                mbar_arrive_cluster_relaxed(tempty_base + 8 * buf);
+            }
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -349,25 +424,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
 
-      // ---- epilogue: BF16 (RNE), swizzled staging, store ----
+      // ---- epilogue: BF16 (RNE) or FP32, swizzled staging, store ----
 #pragma unroll
-      for (int piece = 0; piece < kHalfCols / kEpiCols; ++piece) {
+      for (int piece = 0; piece < kHalfCols / kPieceCols; ++piece) {
         if (!GROUPED) {
           if (lane == 0) tma_store_wait_read_all();  // staging free again
         }
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int c0 = (piece * kEpiCols + j * 8) / 2;
-          __nv_bfloat162 h0 = __float22bfloat162_rn(acc[c0 + 0]);
-          __nv_bfloat162 h1 = __float22bfloat162_rn(acc[c0 + 1]);
-          __nv_bfloat162 h2 = __float22bfloat162_rn(acc[c0 + 2]);
-          __nv_bfloat162 h3 = __float22bfloat162_rn(acc[c0 + 3]);
+          // 16 bytes: 8 BF16 or 4 FP32 outputs of this thread's row
+          const int c0 = (piece * kPieceCols + j * (16 / kOutBytes)) / 2;
           uint4 v;
-          v.x = *reinterpret_cast<uint32_t*>(&h0);
-          v.y = *reinterpret_cast<uint32_t*>(&h1);
-          v.z = *reinterpret_cast<uint32_t*>(&h2);
-          v.w = *reinterpret_cast<uint32_t*>(&h3);
+          if (F32) {
+            v = make_uint4(__float_as_uint(acc[c0].x), __float_as_uint(acc[c0].y), __float_as_uint(acc[c0 + 1].x),
+                           __float_as_uint(acc[c0 + 1].y));
+          } else {
+            __nv_bfloat162 h0 = __float22bfloat162_rn(acc[c0 + 0]);
+            __nv_bfloat162 h1 = __float22bfloat162_rn(acc[c0 + 1]);
+            __nv_bfloat162 h2 = __float22bfloat162_rn(acc[c0 + 2]);
+            __nv_bfloat162 h3 = __float22bfloat162_rn(acc[c0 + 3]);
+            v.x = *reinterpret_cast<uint32_t*>(&h0);
+            v.y = *reinterpret_cast<uint32_t*>(&h1);
+            v.z = *reinterpret_cast<uint32_t*>(&h2);
+            v.w = *reinterpret_cast<uint32_t*>(&h3);
+          }
           // 128-byte swizzle: 16-byte chunk j of row `lane` sits at chunk j ^ (lane % 8)
           *reinterpret_cast<uint4*>(staging_ptr + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
         }
@@ -375,12 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmY, staging, col0 + piece * kEpiCols, a_row + q * 32);
+            tma_store_2d(&tmY, staging, col0 + piece * kPieceCols, a_row + q * 32);
             tma_store_commit();
           }
         } else {
           __syncwarp();
           // 32 rows x 128 bytes: lane reads chunk (lane % 8) of rows lane/8 + 4i
+          uint8_t* ybytes = static_cast<uint8_t*>(p.y);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int r = (lane >> 3) + 4 * i;
@@ -388,8 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 v = *reinterpret_cast<const uint4*>(staging_ptr + r * 128 + ((ch ^ (r & 7)) << 4));
             const int32_t grow = a_row + q * 32 + r;
             if (grow < row_end)
-              *reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(grow) * p.ldy + col0 + piece * kEpiCols + ch * 8) =
-                  v;
+              *reinterpret_cast<uint4*>(ybytes + (static_cast<int64_t>(grow) * p.ldy + col0 + piece * kPieceCols) *
+                                                     kOutBytes +
+                                        ch * 16) = v;
           }
           __syncwarp();
         }
@@ -401,16 +484,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- teardown ----------------
   __syncwarp();
   tc_fence_before_sync();
-  __syncthreads();
+  if (CG > 1)
+    cluster_sync_all();  // no CTA leaves while its peer may still signal it or use its TMEM
+  else
+    __syncthreads();
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) {
+    if (CG == 1)
+      tmem_dealloc(tmem_base, kTmemCols);
+    else
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
 }
 
-template <int BN, int STAGES, bool GROUPED>
+// Largest number of clusters of this kernel variant that can be resident at
+// once on the current device (queried once per device and variant).
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32>
+int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) {
+  static std::atomic<int> cache[64];
+  const int idx = dev.ordinal & 63;
+  int n = cache[idx].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  n = dev.num_sms / CG;
+  if (CG > 1) {
+    int q = 0;
+    if (cudaOccupancyMaxActiveClusters(&q, blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32>, &cfg) == cudaSuccess &&
+        q > 0)
+      n = q;
+    else
+      (void)cudaGetLastError();
+  }
+  cache[idx].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Persistent launch: one cluster of CG CTAs per CG SMs, at most one per
+// cluster tile.
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32>
 cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                          const CUtensorMap& tmY, const Params& p, int grid, cudaStream_t stream) {
-  using L = Smem<BN, STAGES>;
-  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED>;
+                          const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream) {
+  using L = Smem<BN, STAGES, CG>;
+  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32>;
   if (BN == 256) {
     // setmaxnreg.inc only completes if the launch holds kRegsLaunch registers
     // per thread; refuse to launch a build that does not.
@@ -421,14 +535,34 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   }
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, L::kDynamic, stream>>>(tmA, tmB, tmY, p);
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = CG;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::kDynamic;
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(CG, 1, 1);
+  const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32>(dev, cfg);
+  const int64_t clusters = cluster_tiles < resident ? cluster_tiles : resident;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmY, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-constexpr int kStages256 = 4;
-constexpr int kStages128 = 6;
-static_assert(Smem<256, kStages256>::kDynamic <= 232448, "shared memory budget (BN=256)");
-static_assert(Smem<128, kStages128>::kDynamic <= 232448, "shared memory budget (BN=128)");
+constexpr int kStagesPair = 6;   // BN = 256 on a CTA pair: 32 KB stages
+// Whether wide tiles run on CTA pairs (cta_group::2) or single CTAs.
+constexpr bool kUsePairs = true;
+constexpr int kStages256 = 4;    // BN = 256 on one CTA: 48 KB stages
+constexpr int kStages128 = 6;    // BN = 128 on one CTA: 32 KB stages
+static_assert(Smem<256, kStagesPair, 2>::kDynamic <= 232448, "shared memory budget (BN=256, pair)");
+static_assert(Smem<256, kStages256, 1>::kDynamic <= 232448, "shared memory budget (BN=256)");
+static_assert(Smem<128, kStages128, 1>::kDynamic <= 232448, "shared memory budget (BN=128)");
 
 Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const float* sw, void* y, int64_t ldy,
                    int64_t M, int64_t N, int64_t K, const int32_t* offsets, int32_t G) {
@@ -436,7 +570,7 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
   p.sa = sa;
   p.ld_sa = ld_sa;
   p.sw = sw;
-  p.y = static_cast<__nv_bfloat16*>(y);
+  p.y = y;
   p.ldy = ldy;
   p.M = static_cast<int32_t>(M);
   p.N = static_cast<int32_t>(N);
@@ -448,48 +582,70 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
   return p;
 }
 
+
+// Tile shapes: narrow (BN = 128, one CTA), wide (BN = 256, one CTA) and
+// pair (BN = 256 on a CTA pair, 256 x 256 per pair).
+enum class Shape { kNarrow, kWide, kPair };
+
+template <bool GROUPED, bool F32>
+cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                         const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream) {
+  switch (shape) {
+    case Shape::kNarrow:
+      return launch_kernel<128, kStages128, GROUPED, 1, F32>(dev, tmA, tmB, tmY, p, cluster_tiles, stream);
+    case Shape::kWide:
+      return launch_kernel<256, kStages256, GROUPED, 1, F32>(dev, tmA, tmB, tmY, p, cluster_tiles, stream);
+    case Shape::kPair:
+      return launch_kernel<256, kStagesPair, GROUPED, 2, F32>(dev, tmA, tmB, tmY, p, cluster_tiles, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
-                                    int64_t ldy, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+                                    int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
   // Wide tiles (BN = 256) halve the operand traffic per FLOP; narrow ones keep
   // every SM busy when there are few tiles (skinny, decode-shaped M).
   const int64_t m_tiles = (M + BM - 1) / BM;
   const bool wide = (N % 256 == 0) && m_tiles * (N / 256) >= dev.num_sms;
+  const Shape shape = !wide ? Shape::kNarrow : (kUsePairs && m_tiles >= 2 ? Shape::kPair : Shape::kWide);
+  const int CG = shape == Shape::kPair ? 2 : 1;
   const int BN = wide ? 256 : 128;
+  const int out_bytes = y_f32 ? 4 : 2;
   CUtensorMap tmA, tmB, tmY;
   if (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, N, ldqw, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M, ldy * 2, kEpiCols, 32,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, N, ldqw, BK, BN / CG, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tmY, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M,
+                    ldy * out_bytes, kEpiRowBytes / out_bytes, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const Params p = make_params(dev, sa, ld_sa, sw, y, ldy, M, N, K, nullptr, 1);
-  const int64_t tiles = m_tiles * (N / BN);
-  const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
-  if (wide) return launch_kernel<256, kStages256, false>(dev, tmA, tmB, tmY, p, grid, stream);
-  return launch_kernel<128, kStages128, false>(dev, tmA, tmB, tmY, p, grid, stream);
+  const int64_t cluster_tiles = (m_tiles + CG - 1) / CG * (N / BN);
+  return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream)
+               : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream);
 }
 
 cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,
                                             int64_t M_total, const void* qa, int64_t ldqa, const float* sa,
                                             int64_t ld_sa, const void* qw, const float* sw, void* y, int64_t ldy,
-                                            int64_t N, int64_t K, cudaStream_t stream) {
+                                            bool y_f32, int64_t N, int64_t K, cudaStream_t stream) {
   const bool wide = (N % 256 == 0);
+  const Shape shape = !wide ? Shape::kNarrow : (kUsePairs ? Shape::kPair : Shape::kWide);
+  const int CG = shape == Shape::kPair ? 2 : 1;
   const int BN = wide ? 256 : 128;
   CUtensorMap tmA, tmB;
   if (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M_total, ldqa, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, static_cast<uint64_t>(G) * N, K, BK, BN,
+      !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, static_cast<uint64_t>(G) * N, K, BK, BN / CG,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const CUtensorMap& tmY = tmA;  // unused by the grouped epilogue
   const Params p = make_params(dev, sa, ld_sa, sw, y, ldy, M_total, N, K, offsets, G);
-  // Upper bound on the tile count without reading the offsets: every group
-  // can add at most one partial M tile.
-  const int64_t max_tiles = ((M_total + BM - 1) / BM + G) * (N / BN);
-  const int grid = static_cast<int>(max_tiles < dev.num_sms ? max_tiles : dev.num_sms);
-  if (wide) return launch_kernel<256, kStages256, true>(dev, tmA, tmB, tmY, p, grid, stream);
-  return launch_kernel<128, kStages128, true>(dev, tmA, tmB, tmY, p, grid, stream);
+  // Upper bound on the cluster-tile count without reading the offsets: each
+  // group adds at most one partial row tile and one partial cluster tile.
+  const int64_t max_ctiles = (((M_total + BM - 1) / BM + G) / CG + G) * (N / BN);
+  return y_f32 ? launch_shape<true, true>(shape, dev, tmA, tmB, tmY, p, max_ctiles, stream)
+               : launch_shape<true, false>(shape, dev, tmA, tmB, tmY, p, max_ctiles, stream);
 }
 
 }  // namespace fp8bs

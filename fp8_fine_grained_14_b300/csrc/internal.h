@@ -32,14 +32,18 @@ cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, in
                                         void* q, int64_t ldq, float* sw, cudaStream_t stream);
 
 // Returns cudaErrorInvalidValue when a tensor map cannot be encoded.
+// y is BF16 (y_f32 false) or FP32 (y_f32 true); ldy in elements of that type.
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
-                                    int64_t ldy, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+                                    int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,
                                             int64_t M_total, const void* qa, int64_t ldqa, const float* sa,
                                             int64_t ld_sa, const void* qw, const float* sw, void* y, int64_t ldy,
-                                            int64_t N, int64_t K, cudaStream_t stream);
+                                            bool y_f32, int64_t N, int64_t K, cudaStream_t stream);
+
+cudaError_t launch_dequant_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
+                                          const float* sw, void* y, int64_t ldy, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
 

@@ -8,12 +8,14 @@
 // s = 0 and codes 0x00.
 //
 // Both kernels are HBM-bound (2 bytes read, 1 byte + 4/group written per
-// element): 16-byte vector loads, shuffle reductions, packed 8-byte code
-// stores.  Scales use the correctly rounded __fdiv_rn; codes come from a
-// bracketing reciprocal product with an exact-division fallback (see
-// GroupScale).  The build never enables fast math or flush-to-zero, so codes
-// and scales are bit-identical to the float32 definition.
+// element), so the arithmetic per element is kept to a handful of
+// instructions: packed BF16 abs-max, a division-free exact scale, packed FP32
+// products against a bracketing reciprocal, and the hardware E4M3 pair
+// conversion.  The build never enables fast math or flush-to-zero; codes and
+// scales are bit-identical to the float32 definition (see group_scale and
+// quantise8 for why).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -21,113 +23,157 @@
 namespace fp8bs {
 namespace {
 
-constexpr float kE4M3Max = 448.0f;
+// fl32(1 / 448), the float32 nearest to 1/448.
+constexpr float kInv448 = 0x1.24924ap-9f;
+
+// s = fl32(amax / 448) without a division: q = fl32(amax * fl32(1/448)), then
+// one correction with the exact FMA residual amax - 448 q.  amax is always a
+// BF16 value (the largest |x| of BF16 inputs), and this sequence returns the
+// correctly rounded quotient for every non-negative finite BF16 value,
+// subnormals included (verified exhaustively against exact rational
+// arithmetic, and on the GPU by a test that feeds every BF16 magnitude).
+__device__ __forceinline__ float scale_of(float amax) {
+  const float q = __fmul_rn(amax, kInv448);
+  const float r = __fmaf_rn(-q, 448.0f, amax);
+  return __fmaf_rn(r, kInv448, q);
+}
+
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
 
 // Per-group constants of the quantiser.
 //
-// The codes are defined as E4M3_RNE_satfinite(fl32(x / s)).  Dividing every
-// element is the slowest part of the kernel, so each element is first coded
-// from the two bracketing products x * r_lo and x * r_hi, with
-// r = fl32(1 / s) and r_lo / r_hi = r * (1 -/+ 2^-20) rounded.  Each product
-// rounds at most three times by 2^-24 relative, so the pair brackets the
-// correctly rounded quotient with a margin of more than 12 float32 ulps:
-// x * r_lo <= fl32(x / s) <= x * r_hi (order reversed for x < 0).  E4M3
-// rounding with saturation is monotonic, so when both ends give the same code
-// the quotient gives it too.  Only pairs whose bracket straddles a rounding
-// boundary (about 2^-16 of random data) fall back to the IEEE division.
-// Products that underflow keep the sign of x and code to +-0 on both ends,
-// as the quotient does.  Subnormal scales (1 / s would overflow) take the
-// division for the whole group.
+// The codes are E4M3_RNE_satfinite(fl32(x / s)).  Each element is first coded
+// from the two bracketing products x * r_lo and x * r_hi, where r approximates
+// 1 / s to within a few float32 ulps (rcp.approx) and r_lo / r_hi = r * (1 -/+
+// 2^-19), rounded.  With every rounding counted, x * r_lo < fl32(x / s) <
+// x * r_hi for x > 0 (reversed for x < 0) with a margin of more than 2^-21
+// relative.  E4M3 rounding with saturation is monotonic, so when both ends
+// give the same code the quotient gives it too.  Only pairs whose bracket
+// straddles a rounding boundary (about 2^-14 of random data) are recomputed
+// with the IEEE division.  Products that underflow keep the sign of x and
+// code to +-0 at both ends, as the quotient does.  Subnormal scales, whose
+// reciprocal may overflow, take the division for the whole group.
 struct GroupScale {
   float s;
-  float r_lo;
-  float r_hi;
-  bool bracket_ok;  // s is a normal float: the bracketing products are valid
+  float2 r_lo;
+  float2 r_hi;
+  bool bracket_ok;  // s is a normal float32: the bracketing products are valid
 };
 
 __device__ __forceinline__ GroupScale group_scale(float amax) {
   GroupScale g;
-  g.s = __fdiv_rn(amax, kE4M3Max);
+  g.s = scale_of(amax);
   g.bracket_ok = g.s >= 1.17549435e-38f;  // smallest normal float32
-  const float r = __frcp_rn(g.s);
-  g.r_lo = __fmul_rn(r, 1.0f - 0x1p-20f);
-  g.r_hi = __fmul_rn(r, 1.0f + 0x1p-20f);
+  const float r = rcp_approx(g.s);
+  const float lo = __fmul_rn(r, 1.0f - 0x1p-19f);
+  const float hi = __fmul_rn(r, 1.0f + 0x1p-19f);
+  g.r_lo = make_float2(lo, lo);
+  g.r_hi = make_float2(hi, hi);
   return g;
 }
 
-// Codes of two values (a in the low byte) by correctly rounded division.
-__device__ __forceinline__ uint32_t quant_pair_div(float a, float b, float s) {
-  return cvt_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
+// Four E4M3 codes (x0 in the low byte) from four float32 values.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(out)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return out;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t u) {
+  return make_float2(bf16lo_to_f32(u), bf16hi_to_f32(u));
+}
+
+// Codes of 8 values by correctly rounded division (the rare fallback).
+__device__ __noinline__ uint2 quantise8_div(uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __fdiv_rn(bf16lo_to_f32(w[i]), s);
+    f[2 * i + 1] = __fdiv_rn(bf16hi_to_f32(w[i]), s);
+  }
+  return make_uint2(cvt_e4m3x4(f[0], f[1], f[2], f[3]), cvt_e4m3x4(f[4], f[5], f[6], f[7]));
 }
 
 // Quantise 8 BF16 values (one 16-byte vector) of a group into 8 codes.
 __device__ __forceinline__ uint2 quantise8(const uint4 v, const GroupScale& g) {
   if (g.s == 0.0f) return make_uint2(0u, 0u);  // all-zero group
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t pair[4];
-  bool same = true;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = bf16lo_to_f32(w[i]);
-    const float b = bf16hi_to_f32(w[i]);
-    const uint32_t lo = cvt_e4m3x2(__fmul_rn(a, g.r_lo), __fmul_rn(b, g.r_lo));
-    const uint32_t hi = cvt_e4m3x2(__fmul_rn(a, g.r_hi), __fmul_rn(b, g.r_hi));
-    pair[i] = lo;
-    same = same && (lo == hi);
-  }
-  if (!(same && g.bracket_ok)) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) pair[i] = quant_pair_div(bf16lo_to_f32(w[i]), bf16hi_to_f32(w[i]), g.s);
-  }
-  return make_uint2(pair[0] | (pair[1] << 16), pair[2] | (pair[3] << 16));
+  const float2 a = bf16x2_to_f32x2(v.x), b = bf16x2_to_f32x2(v.y);
+  const float2 c = bf16x2_to_f32x2(v.z), d = bf16x2_to_f32x2(v.w);
+  const float2 al = __fmul2_rn(a, g.r_lo), ah = __fmul2_rn(a, g.r_hi);
+  const float2 bl = __fmul2_rn(b, g.r_lo), bh = __fmul2_rn(b, g.r_hi);
+  const float2 cl = __fmul2_rn(c, g.r_lo), ch = __fmul2_rn(c, g.r_hi);
+  const float2 dl = __fmul2_rn(d, g.r_lo), dh = __fmul2_rn(d, g.r_hi);
+  const uint32_t lo0 = cvt_e4m3x4(al.x, al.y, bl.x, bl.y), hi0 = cvt_e4m3x4(ah.x, ah.y, bh.x, bh.y);
+  const uint32_t lo1 = cvt_e4m3x4(cl.x, cl.y, dl.x, dl.y), hi1 = cvt_e4m3x4(ch.x, ch.y, dh.x, dh.y);
+  if (lo0 == hi0 && lo1 == hi1 && g.bracket_ok) return make_uint2(lo0, lo1);
+  return quantise8_div(v, g.s);
 }
 
-__device__ __forceinline__ float absmax8(const uint4 v) {
-  float m = 0.0f;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = fmaxf(m, fabsf(bf16lo_to_f32(w[i])));
-    m = fmaxf(m, fabsf(bf16hi_to_f32(w[i])));
-  }
-  return m;
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
+  __nv_bfloat162 h;
+  *reinterpret_cast<uint32_t*>(&h) = u;
+  return h;
+}
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// Pairwise maxima of |x| over one 16-byte vector (two BF16 lanes).  Clearing
+// the sign bits gives |x|, and the max of non-negative values is exact.
+__device__ __forceinline__ uint32_t absmax8_pairs(const uint4 v) {
+  constexpr uint32_t kMag = 0x7FFF7FFFu;
+  const __nv_bfloat162 m01 = __hmax2(as_bf162(v.x & kMag), as_bf162(v.y & kMag));
+  const __nv_bfloat162 m23 = __hmax2(as_bf162(v.z & kMag), as_bf162(v.w & kMag));
+  return as_u32(__hmax2(m01, m23));
+}
+__device__ __forceinline__ uint32_t max_pairs(uint32_t a, uint32_t b) {
+  return as_u32(__hmax2(as_bf162(a), as_bf162(b)));
+}
+// float32 value of the larger of the two BF16 lanes.
+__device__ __forceinline__ float pairs_to_max(uint32_t m) {
+  return fmaxf(bf16lo_to_f32(m), bf16hi_to_f32(m));
 }
 
 // ---------------------------------------------------------------------------
 // 1x128 activation tiles.
 //
-// A CTA of 256 threads = 16 half-warps works on a tile of 16 rows x UNROLL
-// groups: half-warp h owns row (16*tm + h) and walks UNROLL consecutive
-// 128-channel groups; each of its 16 lanes holds 8 channels of a group.  The
-// UNROLL loads of a thread are issued before any arithmetic.  For a given
-// group, the 16 scales of the tile's rows are 64 contiguous bytes of sa.
+// Grid: x over groups of U consecutive 128-channel groups, y over tiles of 16
+// rows.  A CTA of 256 threads = 16 half-warps; half-warp h owns row
+// (16 * tile + h) and its 16 lanes hold 8 channels each of a group.  The U
+// loads of a thread are issued before any arithmetic.
 // ---------------------------------------------------------------------------
-template <int UNROLL>
+template <int U>
 __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint4* __restrict__ x, int64_t M, int64_t KB,
                                                               int64_t ldx_v, uint2* __restrict__ q, int64_t ldq_v,
                                                               float* __restrict__ sa, int64_t ld_sa) {
   const int lane16 = threadIdx.x & 15;
   const int h = threadIdx.x >> 4;
+  const int64_t kb0 = static_cast<int64_t>(blockIdx.x) * U;
   const int64_t tiles_m = (M + 15) / 16;
-  const int64_t tiles_k = (KB + UNROLL - 1) / UNROLL;
-  const int64_t total = tiles_m * tiles_k;
-  for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-    const int64_t tm = t / tiles_k;
-    const int64_t kb0 = (t - tm * tiles_k) * UNROLL;
+  for (int64_t tm = blockIdx.y; tm < tiles_m; tm += gridDim.y) {
     const int64_t row = tm * 16 + h;
     const bool row_ok = row < M;
-    uint4 v[UNROLL];
+    const uint4* src = x + row * ldx_v + kb0 * 16 + lane16;
+    uint4 v[U];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
+    for (int u = 0; u < U; ++u) {
       v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (row_ok && kb0 + u < KB) v[u] = ld_nc_v4(x + row * ldx_v + (kb0 + u) * 16 + lane16);
+      if (row_ok && kb0 + u < KB) v[u] = ld_nc_v4(src + u * 16);
     }
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      float amax = absmax8(v[u]);
+    for (int u = 0; u < U; ++u) {
+      uint32_t m = absmax8_pairs(v[u]);
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const GroupScale g = group_scale(amax);
+      for (int off = 8; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const GroupScale g = group_scale(pairs_to_max(m));
       const int64_t kb = kb0 + u;
       if (row_ok && kb < KB) {
         q[row * ldq_v + kb * 16 + lane16] = quantise8(v[u], g);
@@ -138,53 +184,116 @@ __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint4* __res
 }
 
 // ---------------------------------------------------------------------------
-// 128x128 weight blocks: one CTA per block.  Thread t holds the 16-byte
-// column slice (t % 16) of rows (t / 16) + 16 i, i = 0..7, i.e. the whole
-// block sits in registers, so the block is read from HBM exactly once.
+// 128x128 weight blocks: one CTA per block (grid x over K blocks, y over N
+// blocks).  Thread t holds the 16-byte column slice (t % 16) of rows
+// (t / 16) + 16 i, i = 0..7, i.e. the whole block sits in registers and is
+// read from HBM exactly once.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256, 3) quant_weight_128x128_kernel(const uint4* __restrict__ w, int64_t NB,
-                                                                   int64_t KB, int64_t ldw_v, uint2* __restrict__ q,
-                                                                   int64_t ldq_v, float* __restrict__ sw) {
-  __shared__ float warp_max[8];
+                                                                      int64_t KB, int64_t ldw_v,
+                                                                      uint2* __restrict__ q, int64_t ldq_v,
+                                                                      float* __restrict__ sw) {
+  __shared__ uint32_t warp_max[8];
   const int c = threadIdx.x & 15;
   const int r0 = threadIdx.x >> 4;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int64_t total = NB * KB;
-  for (int64_t b = blockIdx.x; b < total; b += gridDim.x) {
-    const int64_t nb = b / KB;
-    const int64_t kb = b - nb * KB;
-    const int64_t row0 = nb * 128 + r0;
+  const int64_t kb = blockIdx.x;
+  for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
+    const uint4* src = w + (nb * 128 + r0) * ldw_v + kb * 16 + c;
     uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = ld_nc_v4(w + (row0 + 16 * i) * ldw_v + kb * 16 + c);
-    float amax = 0.0f;
+    for (int i = 0; i < 8; ++i) v[i] = ld_nc_v4(src + 16 * i * ldw_v);
+    uint32_t m = absmax8_pairs(v[0]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, absmax8(v[i]));
+    for (int i = 1; i < 8; ++i) m = max_pairs(m, absmax8_pairs(v[i]));
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) warp_max[warp] = amax;
+    for (int off = 16; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) warp_max[warp] = m;
     __syncthreads();
-    amax = warp_max[0];
+    m = warp_max[0];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
+    for (int i = 1; i < 8; ++i) m = max_pairs(m, warp_max[i]);
     __syncthreads();  // warp_max is reused by the next block of this CTA
-    const GroupScale g = group_scale(amax);
+    const GroupScale g = group_scale(pairs_to_max(m));
     if (threadIdx.x == 0) sw[nb * KB + kb] = g.s;
+    uint2* dst = q + (nb * 128 + r0) * ldq_v + kb * 16 + c;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[(row0 + 16 * i) * ldq_v + kb * 16 + c] = quantise8(v[i], g);
+    for (int i = 0; i < 8; ++i) dst[16 * i * ldq_v] = quantise8(v[i], g);
   }
 }
+
+// ---------------------------------------------------------------------------
+// 128x128 block dequantisation (FP8 codes + block scale -> BF16), the
+// inverse of the weight quantiser: y = bf16_rn(fl32(dec(q) * s)).  E4M3
+// values are exact in FP16, so each code pair is widened with the hardware
+// e4m3x2 -> f16x2 conversion, then to FP32, multiplied by the block scale
+// (one rounding) and rounded to BF16.  One CTA per block (grid x over K
+// blocks, y over N blocks); thread t handles 16 codes (one 16-byte chunk) of
+// rows (t / 8) + 32 i, i = 0..3.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\t"
+      "cvt.u16.u32 c, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "r"(two_codes));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float2 v) {
+  const __nv_bfloat162 b = __float22bfloat162_rn(v);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// 4 codes (one 32-bit word) -> 4 BF16 values (two 32-bit words).
+__device__ __forceinline__ uint2 dequant4(uint32_t codes, float2 s2) {
+  const float2 lo = __fmul2_rn(e4m3x2_to_f32x2(codes & 0xFFFFu), s2);
+  const float2 hi = __fmul2_rn(e4m3x2_to_f32x2(codes >> 16), s2);
+  return make_uint2(bf16x2_rn(lo), bf16x2_rn(hi));
+}
+
+__global__ void __launch_bounds__(256) dequant_weight_128x128_kernel(const uint4* __restrict__ q, int64_t NB,
+                                                                     int64_t KB, int64_t ldq_v,
+                                                                     const float* __restrict__ sw,
+                                                                     uint4* __restrict__ y, int64_t ldy_v) {
+  const int c = threadIdx.x & 7;
+  const int r0 = threadIdx.x >> 3;
+  const int64_t kb = blockIdx.x;
+  for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
+    const float s = __ldg(sw + nb * KB + kb);
+    const float2 s2 = make_float2(s, s);
+    const uint4* src = q + (nb * 128 + r0) * ldq_v + kb * 8 + c;
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = ld_nc_v4(src + 32 * i * ldq_v);
+    uint4* dst = y + (nb * 128 + r0) * ldy_v + kb * 16 + 2 * c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 a = dequant4(v[i].x, s2), b = dequant4(v[i].y, s2);
+      const uint2 d = dequant4(v[i].z, s2), e = dequant4(v[i].w, s2);
+      dst[32 * i * ldy_v] = make_uint4(a.x, a.y, b.x, b.y);
+      dst[32 * i * ldy_v + 1] = make_uint4(d.x, d.y, e.x, e.y);
+    }
+  }
+}
+
+constexpr int64_t kMaxGridY = 65535;
 
 }  // namespace
 
 cudaError_t launch_quant_act_1x128(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx, void* q,
                                    int64_t ldq, float* sa, int64_t ld_sa, cudaStream_t stream) {
-  constexpr int kUnroll = 4;
+  (void)dev;
+  // Two 128-channel groups per thread: small work units keep the last wave of
+  // CTAs short (the grid is several waves of 8 resident CTAs per SM).
+  constexpr int kUnroll = 2;
   const int64_t KB = K / 128;
-  const int64_t tiles = ((M + 15) / 16) * ((KB + kUnroll - 1) / kUnroll);
-  const int64_t resident = static_cast<int64_t>(dev.num_sms) * 8;  // 8 CTAs of 256 threads per SM
-  const int grid = static_cast<int>(tiles < resident ? tiles : resident);
+  const int64_t tiles_m = (M + 15) / 16;
+  const dim3 grid(static_cast<unsigned>((KB + kUnroll - 1) / kUnroll),
+                  static_cast<unsigned>(tiles_m < kMaxGridY ? tiles_m : kMaxGridY));
   quant_act_1x128_kernel<kUnroll><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), M, KB, ldx / 8,
                                                             static_cast<uint2*>(q), ldq / 8, sa, ld_sa);
   return cudaGetLastError();
@@ -192,12 +301,21 @@ cudaError_t launch_quant_act_1x128(const DeviceInfo& dev, const void* x, int64_t
 
 cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, int64_t N, int64_t K, int64_t ldw,
                                         void* q, int64_t ldq, float* sw, cudaStream_t stream) {
+  (void)dev;
   const int64_t NB = N / 128, KB = K / 128;
-  const int64_t blocks = NB * KB;
-  const int64_t cap = static_cast<int64_t>(dev.num_sms) * 64;  // grid-stride beyond this
-  const int grid = static_cast<int>(blocks < cap ? blocks : cap);
+  const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(NB < kMaxGridY ? NB : kMaxGridY));
   quant_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(w), NB, KB, ldw / 8,
                                                         static_cast<uint2*>(q), ldq / 8, sw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
+                                          const float* sw, void* y, int64_t ldy, cudaStream_t stream) {
+  (void)dev;
+  const int64_t NB = N / 128, KB = K / 128;
+  const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(NB < kMaxGridY ? NB : kMaxGridY));
+  dequant_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
+                                                          static_cast<uint4*>(y), ldy / 8);
   return cudaGetLastError();
 }
 

@@ -100,6 +100,16 @@ fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa,
                                   int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
+ * As fp8_blockscaled_gemm, with FP32 output (paragraph 4: the FP8 GEMMs
+ * "produce outputs in BF16 or FP32"): y[m, n] is the FP32 accumulator itself,
+ * not rounded further.  y : [M, N] FP32, row stride ldy (elements, ldy % 4 == 0).
+ */
+fp8bs_status fp8_blockscaled_gemm_f32(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                      const void* qw, int64_t ldqw, const float* sw,
+                                      float* y_f32, int64_t ldy,
+                                      int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * Grouped (per-expert) block-scaled GEMM for MoE row groups.  Rows
  * off[g] .. off[g+1]-1 of qa, sa and y belong to expert g and are multiplied
  * by expert g's weights:
@@ -118,6 +128,28 @@ fp8bs_status fp8_blockscaled_grouped_gemm(int32_t G, const int32_t* group_offset
                                           const void* qw, const float* sw,
                                           void* y_bf16, int64_t ldy,
                                           int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * As fp8_blockscaled_grouped_gemm, with FP32 output (ldy % 4 == 0).
+ */
+fp8bs_status fp8_blockscaled_grouped_gemm_f32(int32_t G, const int32_t* group_offsets_dev, int64_t M_total,
+                                              const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                              const void* qw, const float* sw,
+                                              float* y_f32, int64_t ldy,
+                                              int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * 128x128 block dequantisation, the inverse of fp8_quant_weight_128x128: the
+ * BF16 conversion of FP8 weights that the DeepSeek-V3 model card (section 6,
+ * "How to Run Locally") provides for its FP8-only checkpoints.
+ *   qw : [N, K] E4M3 codes, row stride ldq (bytes).
+ *   sw : [N/128, K/128] FP32 block scales, row-major, contiguous (4-byte aligned).
+ *   y  : [N, K] BF16 out, row stride ldy (elements):
+ *        y[n, k] = bf16_rn(fl32(dec(qw[n, k]) * sw[n/128][k/128])).
+ * N % 128 == 0, K % 128 == 0.  A stack of experts passes as [G*N, K].
+ */
+fp8bs_status fp8_dequant_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, const float* sw,
+                                        void* y_bf16, int64_t ldy, cudaStream_t stream);
 
 /*
  * Text naming the CUDA error (and the step) behind the last FP8BS_ERR_CUDA

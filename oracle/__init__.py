@@ -8,7 +8,9 @@ from .fp8_oracle import (  # noqa: F401
     GROUP,
     blockscaled_gemm,
     blockscaled_grouped_gemm,
+    bf16_round,
     dequant_weight_128x128,
+    dequant_weight_128x128_bf16,
     e4m3_decode,
     e4m3_encode_rne_satfinite,
     fl32_div,

@@ -180,6 +180,30 @@ def dequant_weight_128x128(qw, sw):
     return e4m3_decode(qw) * scale
 
 
+def bf16_round(v) -> np.ndarray:
+    """float32 -> nearest BF16 value (ties to the even BF16 significand),
+    returned as float32.  BF16 keeps the top 16 bits of a float32; rounding
+    adds half a BF16 ulp minus one, plus the parity of the kept LSB, before
+    truncating.  Finite inputs only."""
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return (r.astype(np.uint32) << 16).view(np.float32)
+
+
+def dequant_weight_128x128_bf16(qw, sw):
+    """BF16 weights back from 128x128-quantised codes: for each element,
+    bf16(fl32(dec(q) * s)) with s its block's scale -- the float32 product of
+    the exact code value and the scale, rounded to BF16: the FP8-to-BF16
+    weight conversion that the DeepSeek-V3 model card (section 6, "How to Run
+    Locally") offers for its FP8-only release.  Reading: the product is
+    formed in float32 and rounded to nearest even BF16.
+    Returns float32 [N, K] holding BF16 values."""
+    qw = np.asarray(qw, dtype=np.uint8)
+    scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float32), GROUP, axis=0), GROUP, axis=1)
+    prod = e4m3_decode(qw).astype(np.float32) * scale  # float32 multiply, rounded once
+    return bf16_round(prod)
+
+
 # ---------------------------------------------------------------------------
 # Block-scaled GEMM with per-128-K-chunk promotion.
 # ---------------------------------------------------------------------------

@@ -464,6 +464,52 @@ def pin_grouped(o):
     assert np.array_equal(qst.reshape(G, N, K), qw) and np.array_equal(sst.reshape(G, N // 128, K // 128), sw)
 
 
+# ---------------------------------------------------------------------------
+# Block dequantisation (FP8 -> BF16 weights)
+# ---------------------------------------------------------------------------
+
+def pin_bf16_round(o):
+    """Round-to-nearest-even BF16 against torch's float32 -> bfloat16 cast
+    (an independent library routine) on structured bit patterns: every
+    exponent, and low halves at and around the rounding midpoint 0x8000."""
+    import torch
+
+    exps = np.arange(1, 255, dtype=np.uint32)
+    hi = np.array([0x000, 0x001, 0x07E, 0x07F, 0x040, 0x041], dtype=np.uint32)
+    lo = np.array([0x0000, 0x0001, 0x7FFF, 0x8000, 0x8001, 0xFFFF], dtype=np.uint32)
+    bits = ((exps[:, None, None] << 23) | (hi[None, :, None] << 16) | lo[None, None, :]).ravel()
+    v = bits.view(np.float32)
+    v = np.concatenate([v, -v, np.array([0.0, -0.0], dtype=np.float32)])
+    v = v[np.isfinite(v) & (np.abs(v) < 3.3e38)]
+    want = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    got = o.bf16_round(v)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def pin_dequant_roundtrip(o):
+    """dequant(quant(W)) reproduces W to within half an E4M3 ulp of the block
+    (times its scale) plus the BF16 rounding; codes 0x7E with s = 1.5 give
+    exactly 672; an all-zero block gives zeros."""
+    rng = np.random.default_rng(41)
+    w = (rng.standard_normal((256, 384)) * 0.02).astype(np.float32)
+    w[128:256, 0:128] = 0.0
+    qw, sw = o.quant_weight_128x128(w)
+    y = o.dequant_weight_128x128_bf16(qw, sw).astype(np.float64)
+    s = np.repeat(np.repeat(sw.astype(np.float64), 128, 0), 128, 1)
+    v = np.abs(w.astype(np.float64)) / np.where(s > 0, s, 1)
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
+    ulp = np.where(v < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
+    bound = 0.5 * ulp * s * (1 + 2.0 ** -20) + np.abs(w) * 2.0 ** -8 + 1e-300
+    assert np.all(np.abs(y - w) <= bound)
+    assert np.all(y[128:256, 0:128] == 0.0)
+    q = np.full((128, 128), 0x7E, dtype=np.uint8)
+    assert np.all(o.dequant_weight_128x128_bf16(q, np.array([[1.5]], dtype=np.float32)) == 672.0)
+    # the float32 product is rounded to BF16 once more: 0x39 (1.125) * 1.0078125 = 1.1337890625 -> 1.1328125
+    q = np.full((128, 128), 0x39, dtype=np.uint8)
+    got = o.dequant_weight_128x128_bf16(q, np.array([[1.0078125]], dtype=np.float32))
+    assert np.all(got == np.float32(1.1328125)), got[0, 0]
+
+
 ALL_PINS = [
     pin_codec_format_points,
     pin_codec_roundtrip,
@@ -486,4 +532,6 @@ ALL_PINS = [
     pin_gemm_linearity,
     pin_gemm_rows_columns,
     pin_grouped,
+    pin_bf16_round,
+    pin_dequant_roundtrip,
 ]

@@ -94,6 +94,20 @@ def test_gemm_validation(lib, args, expect):
 
 
 @pytest.mark.parametrize("args,expect", [
+    ((A16, 128, 100, 128, A16, A16, 128, None), 3),      # K % 128
+    ((A16, 0, 128, 128, A16, A16, 128, None), 3),        # N == 0
+    ((A16, 128, 128, 64, A16, A16, 128, None), 1),       # ldq < K
+    ((A16, 128, 128, 128, A16, A16, 64, None), 1),       # ldy < K
+    ((None, 128, 128, 128, A16, A16, 128, None), 1),     # null codes
+    ((A16, 128, 128, 136, A16, A16, 128, None), 2),      # ldq % 16
+    ((A16, 128, 128, 128, A16, P(0x10008), 128, None), 2),  # misaligned y
+    ((A16, 128, 128, 128, P(0x10002), A16, 128, None), 2),  # misaligned scales
+])
+def test_dequant_validation(lib, args, expect):
+    assert lib.fp8_dequant_weight_128x128(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
     ((0, A16, 10, A16, 128, A16, 12, A16, A16, A16, 128, 128, 128, None), 1),      # G == 0
     ((2, None, 10, A16, 128, A16, 12, A16, A16, A16, 128, 128, 128, None), 1),     # null offsets
     ((2, A16, 10, A16, 128, A16, 12, A16, A16, A16, 128, 100, 128, None), 3),      # N % 128

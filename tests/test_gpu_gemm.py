@@ -137,3 +137,41 @@ def test_full_size_sampled(name):
     assert_scales_equal(f32(sw)[blocks], sw_r, "sw")
     ysub = y[torch.as_tensor(rows, device=DEV)][:, torch.as_tensor(cols, device=DEV)]
     assert_gemm_close(f32(ysub), y_ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 384, 256), (300, 512, 640), (1300, 4096, 384), (64, 1024, 1024)])
+def test_f32_output(M, N, K):
+    """FP32 output ("outputs in BF16 or FP32", paragraph 4): within the GEMM
+    tolerance of the oracle, and the BF16 output is exactly its RNE rounding
+    (both epilogues read the same FP32 accumulator)."""
+    x, w = workloads.dense_inputs(M, N, K, seed=M + 5 * N + K)
+    xd, wd = x.to(DEV), w.to(DEV)
+    qa, sa = fb.fp8_quant_act_1x128(xd)
+    qw, sw = fb.fp8_quant_weight_128x128(wd)
+    y32 = fb.fp8_blockscaled_gemm(qa, sa, qw, sw, out_dtype=torch.float32)
+    y16 = fb.fp8_blockscaled_gemm(qa, sa, qw, sw)
+    torch.cuda.synchronize()
+    assert y32.dtype == torch.float32
+    y_ref, _ = oracle.linear_forward(f32(x), f32(w))
+    assert_gemm_close(f32(y32), y_ref)
+    assert np.array_equal(oracle.bf16_round(f32(y32)).view(np.uint32), f32(y16).view(np.uint32))
+    assert fb.fp8bs_last_device_error() == 0
+
+
+def test_f32_output_strided_and_full_size_sampled():
+    x, w = workloads.config_inputs("up")
+    xd, wd = x.to(DEV), w.to(DEV)
+    qa, sa = fb.fp8_quant_act_1x128(xd)
+    qw, sw = fb.fp8_quant_weight_128x128(wd)
+    M, N = x.shape[0], w.shape[0]
+    ybig = torch.full((M, N + 32), -1.0, dtype=torch.float32, device=DEV)
+    fb.fp8_blockscaled_gemm(qa, sa, qw, sw, y=ybig[:, :N])
+    y16 = fb.fp8_blockscaled_gemm(qa, sa, qw, sw)
+    torch.cuda.synchronize()
+    assert torch.all(ybig[:, N:] == -1.0)
+    rows = sample_rows(M, 128, seed=31)
+    blocks = sample_blocks(N // 128, 4, seed=32)
+    _, _, _, _, y_ref, cols = oracle_dense_sampled(x, w, rows, blocks)
+    sub = ybig[torch.as_tensor(rows, device=DEV)][:, torch.as_tensor(cols, device=DEV)]
+    assert_gemm_close(f32(sub), y_ref)
+    assert np.array_equal(oracle.bf16_round(f32(ybig[:, :N])).view(np.uint32), f32(y16).view(np.uint32))

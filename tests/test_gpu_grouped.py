@@ -53,6 +53,24 @@ def test_grouped_small(counts, N, K):
     assert_gemm_close(f32(y), y_ref)
 
 
+def test_grouped_f32_output():
+    counts = [77, 300, 0, 129, 5]
+    G, N, K = len(counts), 512, 384
+    offsets = workloads.grouped_offsets(counts)
+    x, _ = workloads.dense_inputs(int(offsets[-1]), 128, K, seed=3)
+    _, w = workloads.dense_inputs(1, G * N, K, seed=4)
+    w = w.reshape(G, N, K)
+    y16, qa, sa, qw, sw = _grouped_gpu(offsets, x, w)
+    y32 = fb.fp8_blockscaled_grouped_gemm(offsets.to(DEV), int(offsets[-1]), qa, sa, qw, sw, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    qa_r, sa_r = oracle.quant_act_1x128(f32(x))
+    qw_r, sw_r = oracle.quant_weight_128x128(f32(w).reshape(G * N, K))
+    y_ref = oracle.blockscaled_grouped_gemm(offsets.numpy(), qa_r, sa_r, qw_r.reshape(G, N, K),
+                                            sw_r.reshape(G, N // 128, K // 128))
+    assert_gemm_close(f32(y32), y_ref)
+    assert np.array_equal(oracle.bf16_round(f32(y32)).view(np.uint32), f32(y16).view(np.uint32))
+
+
 def test_grouped_bad_offsets_reported():
     """A decreasing offset table is detected on the device and reported."""
     N, K = 128, 128

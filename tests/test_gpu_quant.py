@@ -165,6 +165,22 @@ def test_weight_quant_near_ties_inexact_scale():
     _weight_parity(w)
 
 
+def test_act_quant_every_bf16_magnitude():
+    """One 1x128 group per positive finite BF16 value (subnormals included):
+    the group's amax takes every value a BF16 input can produce, so the
+    scale s = fl32(amax / 448) is checked for all of them bit for bit."""
+    bits = np.arange(1, 0x7F80, dtype=np.uint32)
+    amax = (bits << 16).view(np.float32)
+    rng = np.random.default_rng(7)
+    x = (rng.uniform(-1.0, 1.0, (len(bits), 128)) * amax[:, None].astype(np.float64)).astype(np.float32)
+    x = f32(torch.from_numpy(x).to(torch.bfloat16))          # BF16 rounding never exceeds amax
+    pos = rng.integers(0, 128, len(bits))
+    sign = np.where(rng.random(len(bits)) < 0.5, -1.0, 1.0).astype(np.float32)
+    x[np.arange(len(bits)), pos] = sign * amax
+    assert np.array_equal(np.max(np.abs(x), axis=1), amax)
+    _act_parity(torch.from_numpy(x).to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("M,K", [(4096, 4096)])
 def test_act_quant_random_sweep(M, K):
     """16.7M elements with a random power-of-two magnitude per row: every code

@@ -69,6 +69,15 @@ MUTANTS = {
     "negated_product": (
         "chunk = a @ b.T",
         "chunk = -(a @ b.T)"),
+    "bf16_round_truncates": (
+        "r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16",
+        "r = u >> 16"),
+    "bf16_round_ties_away": (
+        "r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16",
+        "r = (u + 0x8000) >> 16"),
+    "dequant_scale_of_first_block": (
+        "scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float32), GROUP, axis=0), GROUP, axis=1)",
+        "scale = np.full(qw.shape, np.asarray(sw, dtype=np.float32).flat[0], dtype=np.float32)"),
     "grouped_wrong_weight_scales": (
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])",
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[0])"),
