@@ -14,6 +14,10 @@ _API = (
     "fp8_blockscaled_gemm",
     "fp8_blockscaled_grouped_gemm",
     "fp8_dequant_weight_128x128",
+    "fp8_quant_act_1x128_t",
+    "fp8_transpose_weight_128x128",
+    "fp8_blockscaled_gemm_rowscaled",
+    "linear_backward",
     "fp8bs_last_device_error",
     "fp8bs_set_wait_timeout_ns",
     "fp8bs_selftest_wait_timeout",

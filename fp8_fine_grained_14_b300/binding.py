@@ -35,6 +35,11 @@ EXPORTS = {
     "fp8_blockscaled_gemm_f32": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_grouped_gemm_f32": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
     "fp8_dequant_weight_128x128": [_p, _i64, _i64, _i64, _p, _p, _i64, _p],
+    "fp8_quant_act_1x128_t": [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
+    "fp8_transpose_weight_128x128": [_p, _i64, _i64, _i64, _p, _p, _i64, _p, _p],
+    "fp8_blockscaled_gemm_rowscaled": [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64, _p],
+    "fp8_blockscaled_gemm_rowscaled_f32": [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64,
+                                           _p],
     "fp8bs_status_string": [ctypes.c_int],
     "fp8bs_last_error_detail": [],
     "fp8bs_last_device_error": [_p],
@@ -195,6 +200,75 @@ def fp8_dequant_weight_128x128(qw, sw, y=None, stream=None):
     st = lib.fp8_dequant_weight_128x128(_ptr(qw), N, K, qw.stride(0), _ptr(sw), _ptr(y), y.stride(0), _stream(stream))
     _check("fp8_dequant_weight_128x128", st)
     return y
+
+
+def fp8_quant_act_1x128_t(x, qt=None, st=None, stream=None):
+    """x bf16 [M, K] -> (qt uint8 [K, M] codes of x^T, st float32 [M/128, K]
+    scales): 1x128 tiles of x^T.  M % 128 == 0."""
+    _require(x, torch.bfloat16, "x", 2)
+    M, K = x.shape
+    if qt is None:
+        qt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    if st is None:
+        st = torch.empty((M // 128, ld_sa_for(K)), dtype=torch.float32, device=x.device)
+    _require(qt, torch.uint8, "qt", 2)
+    _require(st, torch.float32, "st", 2)
+    status = lib.fp8_quant_act_1x128_t(_ptr(x), M, K, x.stride(0), _ptr(qt), qt.stride(0), _ptr(st), st.stride(0),
+                                       _stream(stream))
+    _check("fp8_quant_act_1x128_t", status)
+    return qt, st
+
+
+def fp8_transpose_weight_128x128(qw, sw, qwt=None, swt=None, stream=None):
+    """(qw uint8 [N, K], sw [N/128, K/128]) -> (qw^T [K, N], sw^T [K/128, N/128])."""
+    _require(qw, torch.uint8, "qw", 2)
+    N, K = qw.shape
+    if qwt is None:
+        qwt = torch.empty((K, N), dtype=torch.uint8, device=qw.device)
+    if swt is None:
+        swt = torch.empty((K // 128, N // 128), dtype=torch.float32, device=qw.device)
+    _require(qwt, torch.uint8, "qwt", 2)
+    if not sw.is_contiguous() or not swt.is_contiguous():
+        raise ValueError("sw and swt must be contiguous")
+    status = lib.fp8_transpose_weight_128x128(_ptr(qw), N, K, qw.stride(0), _ptr(sw), _ptr(qwt), qwt.stride(0),
+                                              _ptr(swt), _stream(stream))
+    _check("fp8_transpose_weight_128x128", status)
+    return qwt, swt
+
+
+def fp8_blockscaled_gemm_rowscaled(qa, sa, qb, sb, y=None, stream=None, out_dtype=torch.bfloat16):
+    """Y [M, N] = sum_kb sa[kb, m] sb[kb, n] (chunk kb of dec(qa) dec(qb)^T):
+    1x128 scales on both operands (the weight-gradient GEMM)."""
+    _require(qa, torch.uint8, "qa", 2)
+    _require(qb, torch.uint8, "qb", 2)
+    _require(sa, torch.float32, "sa", 2)
+    _require(sb, torch.float32, "sb", 2)
+    M, K = qa.shape
+    N = qb.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=out_dtype, device=qa.device)
+    if y.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("y must be bfloat16 or float32")
+    _require(y, y.dtype, "y", 2)
+    fn = "fp8_blockscaled_gemm_rowscaled" if y.dtype == torch.bfloat16 else "fp8_blockscaled_gemm_rowscaled_f32"
+    status = getattr(lib, fn)(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb), qb.stride(0), _ptr(sb),
+                              sb.stride(0), _ptr(y), y.stride(0), M, N, K, _stream(stream))
+    _check(fn, status)
+    return y
+
+
+def linear_backward(x, w, dy, stream=None, grad_dtype=torch.float32):
+    """Both backward GEMMs of the FP8 linear layer, all in the library's
+    kernels: dX = Q(dY) . Q(W)^T-blocks (BF16) and dW = Q(dY^T) . Q(X^T)^T
+    (FP32 by default).  Returns (dx, dw)."""
+    qw, sw = fp8_quant_weight_128x128(w, stream=stream)
+    qwt, swt = fp8_transpose_weight_128x128(qw, sw, stream=stream)
+    qdy, sdy = fp8_quant_act_1x128(dy, stream=stream)
+    dx = fp8_blockscaled_gemm(qdy, sdy, qwt, swt, stream=stream)
+    qdyt, sdyt = fp8_quant_act_1x128_t(dy, stream=stream)
+    qxt, sxt = fp8_quant_act_1x128_t(x, stream=stream)
+    dw = fp8_blockscaled_gemm_rowscaled(qdyt, sdyt, qxt, sxt, stream=stream, out_dtype=grad_dtype)
+    return dx, dw
 
 
 def fp8bs_last_device_error(stream=None):

@@ -236,9 +236,79 @@ fp8bs_status grouped_gemm(int32_t G, const int32_t* group_offsets_dev, int64_t M
   return e == cudaSuccess ? FP8BS_OK : cuda_failure(name, e);
 }
 
+fp8bs_status rowscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qb,
+                           int64_t ldqb, const float* sb, int64_t ld_sb, void* y, int64_t ldy, int out_bytes,
+                           int64_t M, int64_t N, int64_t K, cudaStream_t stream, const char* name) {
+  if (M < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldqb < 0 || ld_sb < 0 || ldy < 0)
+    return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldqa < K || ldqb < K || ldy < N || ld_sa < M || ld_sb < N) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (qa == nullptr || sa == nullptr || qb == nullptr || sb == nullptr || y == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb) || !aligned16(y) || ldqa % 16 != 0 ||
+      ldqb % 16 != 0 || (ldy * out_bytes) % 16 != 0 || ld_sa % 4 != 0 || ld_sb % 4 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_blockscaled_gemm_rowscaled(*dev, qa, ldqa, sa, ld_sa, qb, ldqb, sb, ld_sb, y, ldy, out_bytes == 4,
+                                               M, N, K, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure(name, e);
+}
+
 }  // namespace
 
 extern "C" {
+
+fp8bs_status fp8_blockscaled_gemm_rowscaled(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                            const void* qb, int64_t ldqb, const float* sb, int64_t ld_sb,
+                                            void* y_bf16, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                            cudaStream_t stream) {
+  return rowscaled_gemm(qa, ldqa, sa, ld_sa, qb, ldqb, sb, ld_sb, y_bf16, ldy, 2, M, N, K, stream,
+                        "fp8_blockscaled_gemm_rowscaled launch");
+}
+
+fp8bs_status fp8_blockscaled_gemm_rowscaled_f32(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                                const void* qb, int64_t ldqb, const float* sb, int64_t ld_sb,
+                                                float* y_f32, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                                cudaStream_t stream) {
+  return rowscaled_gemm(qa, ldqa, sa, ld_sa, qb, ldqb, sb, ld_sb, y_f32, ldy, 4, M, N, K, stream,
+                        "fp8_blockscaled_gemm_rowscaled_f32 launch");
+}
+
+fp8bs_status fp8_quant_act_1x128_t(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* qt, int64_t ldqt,
+                                   float* st, int64_t ld_st, cudaStream_t stream) {
+  if (M < 0 || K < 0 || ldx < 0 || ldqt < 0 || ld_st < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || M % 128 != 0 || K > kMaxDim || M > kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K || ldqt < M || ld_st < K) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (x_bf16 == nullptr || qt == nullptr || st == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(qt) || !aligned16(st) || ldx % 8 != 0 || ldqt % 16 != 0 || ld_st % 4 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_quant_act_1x128_t(*dev, x_bf16, M, K, ldx, qt, ldqt, st, ld_st, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_act_1x128_t launch", e);
+}
+
+fp8bs_status fp8_transpose_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, const float* sw,
+                                          void* qwt, int64_t ldqt, float* swt, cudaStream_t stream) {
+  if (N < 0 || K < 0 || ldq < 0 || ldqt < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldq < K || ldqt < N) return FP8BS_ERR_INVALID_ARG;
+  if (qw == nullptr || sw == nullptr || qwt == nullptr || swt == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qw) || !aligned16(qwt) || (reinterpret_cast<uintptr_t>(sw) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(swt) & 3u) != 0 || ldq % 16 != 0 || ldqt % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_transpose_weight_128x128(*dev, qw, N, K, ldq, sw, qwt, ldqt, swt, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_transpose_weight_128x128 launch", e);
+}
 
 fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,
                                   int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,

@@ -1,0 +1,205 @@
+// backward.cu — operand preparation for the backward GEMMs of the FP8 linear
+// layer on sm_103a.
+//
+// Method ("The Definitive Information To Deepseek"): the activation is kept in
+// FP8 for the backward pass of the linear layer (paragraph 2) and the backward
+// is split into its input-gradient and weight-gradient parts (paragraph 3),
+// both run as FP8 GEMMs with the 1x128 / 128x128 grouping of "Figure 7 (a)".
+//   dX = dY . W     needs W^T: a 128x128 block is a block either way round,
+//                   so the codes and scales of W are transposed, not requantised
+//                   (transpose_weight_128x128_kernel);
+//   dW = dY^T . X   reduces over tokens, so dY and X are quantised on 1x128
+//                   tiles of their transposes, i.e. per channel per 128 tokens
+//                   (quant_act_1x128_t_kernel), and multiplied by the row-scaled
+//                   GEMM (gemm.cu).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant_common.cuh"
+
+namespace fp8bs {
+namespace {
+
+// ---------------------------------------------------------------------------
+// 1x128 quantisation of X^T.  Tiles of 128 rows (tokens) x 128 columns
+// (channels) of X arrive by TMA in a 3-stage ring (persistent CTAs, two per
+// SM).  Thread t owns the column pair cp = t % 64 (channels 2cp, 2cp+1) over
+// the 32 rows 32 * (t / 64) ..; per-column maxima combine across the four row
+// quarters through shared memory; each thread then codes its 2 x 32 values and
+// writes them as two 32-byte runs of X^T's rows.  Scales go to
+// s[m / 128][k] (the activation-scale layout of X^T).
+// ---------------------------------------------------------------------------
+constexpr int kTStages = 3;
+constexpr int kTTileBytes = 128 * 128 * 2;
+constexpr int kTSmem = kTStages * kTTileBytes + kTStages * 8 + 4 * 64 * 4 + 1024;
+
+// Gather 8 BF16 values of one column (low or high halves of 8 packed pairs).
+__device__ __forceinline__ uint4 column8(const uint32_t* r, bool high) {
+  const uint32_t sel = high ? 0x7632u : 0x5410u;
+  return make_uint4(__byte_perm(r[0], r[1], sel), __byte_perm(r[2], r[3], sel), __byte_perm(r[4], r[5], sel),
+                    __byte_perm(r[6], r[7], sel));
+}
+
+__global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                   int64_t MB, int64_t KB, uint4* __restrict__ q,
+                                                                   int64_t ldq_v, float* __restrict__ s,
+                                                                   int64_t ld_s, unsigned* status,
+                                                                   uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  const uint32_t bar_full = base + kTStages * kTTileBytes;
+  uint32_t* quarter_max = reinterpret_cast<uint32_t*>(smem + kTStages * kTTileBytes + kTStages * 8);  // [4][64]
+
+  const int64_t tiles = MB * KB;
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int cp = threadIdx.x & 63;
+  const int rq = threadIdx.x >> 6;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kTStages; ++st) mbar_init(bar_full + 8 * st, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    for (int st = 0; st < kTStages; ++st) {
+      const int64_t t = first + st * stride;
+      if (t >= tiles) break;
+      mbar_arrive_expect_tx(bar_full + 8 * st, kTTileBytes);
+      tma_load_2d(base + st * kTTileBytes, &tmX, bar_full + 8 * st, static_cast<int32_t>((t % KB) * 128),
+                  static_cast<int32_t>((t / KB) * 128));
+    }
+  }
+  __syncthreads();
+
+  int64_t i = 0;
+  for (int64_t t = first; t < tiles; t += stride, ++i) {
+    const int st = static_cast<int>(i % kTStages);
+    const uint32_t parity = static_cast<uint32_t>((i / kTStages) & 1);
+    const bool landed = mbar_wait(bar_full + 8 * st, parity, nullptr, timeout_ns);
+    if (!__syncthreads_and(landed)) {
+      if (threadIdx.x == 0) {
+        record_status(status, kStatusTimeout);
+        for (int k = 0; k < kTStages; ++k) {
+          const int64_t j = i + k;
+          if (first + j * stride >= tiles) break;
+          (void)mbar_wait(bar_full + 8 * (j % kTStages), static_cast<uint32_t>((j / kTStages) & 1), nullptr,
+                          timeout_ns);
+        }
+      }
+      return;
+    }
+    const int64_t mb = t / KB, kb = t % KB;
+    const uint8_t* tile = smem + st * kTTileBytes;
+    uint32_t r[32];  // rows 32 rq + j, columns 2cp (low half) and 2cp + 1 (high half)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = *reinterpret_cast<const uint32_t*>(tile + (32 * rq + j) * 256 + cp * 4);
+    uint32_t m = r[0] & 0x7FFF7FFFu;
+#pragma unroll
+    for (int j = 1; j < 32; ++j) m = max_pairs(m, r[j] & 0x7FFF7FFFu);
+    quarter_max[rq * 64 + cp] = m;
+    __syncthreads();  // quarter maxima visible; stage st fully read into registers
+    if (threadIdx.x == 0) {
+      const int64_t tn = t + kTStages * stride;
+      if (tn < tiles) {
+        mbar_arrive_expect_tx(bar_full + 8 * st, kTTileBytes);
+        tma_load_2d(base + st * kTTileBytes, &tmX, bar_full + 8 * st, static_cast<int32_t>((tn % KB) * 128),
+                    static_cast<int32_t>((tn / KB) * 128));
+      }
+    }
+    m = max_pairs(max_pairs(quarter_max[cp], quarter_max[64 + cp]),
+                  max_pairs(quarter_max[128 + cp], quarter_max[192 + cp]));
+    const GroupScale g_lo = group_scale(bf16lo_to_f32(m));
+    const GroupScale g_hi = group_scale(bf16hi_to_f32(m));
+    const int64_t k0 = kb * 128 + 2 * cp;
+    // X^T rows k0 and k0 + 1, tokens mb * 128 + 32 rq .. + 31: two 16-byte stores each
+    uint4* dst_lo = q + k0 * ldq_v + mb * 8 + rq * 2;
+    uint4* dst_hi = dst_lo + ldq_v;
+    const uint2 a0 = quantise8(column8(r + 0, false), g_lo), a1 = quantise8(column8(r + 8, false), g_lo);
+    const uint2 a2 = quantise8(column8(r + 16, false), g_lo), a3 = quantise8(column8(r + 24, false), g_lo);
+    dst_lo[0] = make_uint4(a0.x, a0.y, a1.x, a1.y);
+    dst_lo[1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
+    const uint2 b0 = quantise8(column8(r + 0, true), g_hi), b1 = quantise8(column8(r + 8, true), g_hi);
+    const uint2 b2 = quantise8(column8(r + 16, true), g_hi), b3 = quantise8(column8(r + 24, true), g_hi);
+    dst_hi[0] = make_uint4(b0.x, b0.y, b1.x, b1.y);
+    dst_hi[1] = make_uint4(b2.x, b2.y, b3.x, b3.y);
+    if (rq == 0) *reinterpret_cast<float2*>(s + mb * ld_s + k0) = make_float2(g_lo.s, g_hi.s);
+    __syncthreads();  // quarter_max is rewritten for the next tile
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 128x128 code blocks of W [N, K] -> W^T [K, N], and the block-scale matrix
+// transposed.  One CTA per block: 16-byte loads into shared memory (row
+// stride padded to 144 bytes), then thread t assembles output row t / 2, bytes
+// 64 (t % 2) .. + 63, from one column of the staged block.
+// ---------------------------------------------------------------------------
+constexpr int kPad = 144;
+
+__global__ void __launch_bounds__(256) transpose_weight_128x128_kernel(const uint4* __restrict__ q, int64_t NB,
+                                                                       int64_t KB, int64_t ldq_v,
+                                                                       const float* __restrict__ sw,
+                                                                       uint4* __restrict__ qt, int64_t ldqt_v,
+                                                                       float* __restrict__ swt) {
+  __shared__ __align__(16) uint8_t blk[128 * kPad];
+  const int64_t kb = blockIdx.x;
+  for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = threadIdx.x + 256 * i;  // 1024 chunks of 16 bytes
+      const int row = idx >> 3, ch = idx & 7;
+      *reinterpret_cast<uint4*>(blk + row * kPad + ch * 16) = ld_nc_v4(q + (nb * 128 + row) * ldq_v + kb * 8 + ch);
+    }
+    __syncthreads();
+    const int j = threadIdx.x >> 1;         // output row within the block (= input column)
+    const int i0 = (threadIdx.x & 1) * 64;  // first input row gathered
+    uint4* dst = qt + (kb * 128 + j) * ldqt_v + nb * 8 + (threadIdx.x & 1) * 4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + 16 * c + 4 * e;
+        w[e] = static_cast<uint32_t>(blk[i * kPad + j]) | (static_cast<uint32_t>(blk[(i + 1) * kPad + j]) << 8) |
+               (static_cast<uint32_t>(blk[(i + 2) * kPad + j]) << 16) |
+               (static_cast<uint32_t>(blk[(i + 3) * kPad + j]) << 24);
+      }
+      dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (threadIdx.x == 0) swt[kb * NB + nb] = sw[nb * KB + kb];
+    __syncthreads();  // blk is refilled for the next block of this CTA
+  }
+}
+
+constexpr int64_t kMaxGridY = 65535;
+
+}  // namespace
+
+cudaError_t launch_quant_act_1x128_t(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     void* qt, int64_t ldqt, float* st, int64_t ld_st, cudaStream_t stream) {
+  const int64_t MB = M / 128, KB = K / 128;
+  CUtensorMap tmX;
+  if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(quant_act_1x128_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = MB * KB;
+  const int64_t resident = static_cast<int64_t>(dev.num_sms) * 2;
+  const int grid = static_cast<int>(tiles < resident ? tiles : resident);
+  quant_act_1x128_t_kernel<<<grid, 256, kTSmem, stream>>>(tmX, MB, KB, static_cast<uint4*>(qt), ldqt / 16, st,
+                                                          ld_st, dev.status, wait_timeout_ns());
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
+                                            const float* sw, void* qt, int64_t ldqt, float* swt,
+                                            cudaStream_t stream) {
+  (void)dev;
+  const int64_t NB = N / 128, KB = K / 128;
+  const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(NB < kMaxGridY ? NB : kMaxGridY));
+  transpose_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
+                                                            static_cast<uint4*>(qt), ldqt / 16, swt);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8bs

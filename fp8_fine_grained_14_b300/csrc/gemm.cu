@@ -76,7 +76,9 @@ struct RegSplit {
 struct Params {
   const float* sa;
   int64_t ld_sa;
-  const float* sw;
+  const float* sw;        // 128x128 block scales of B (unless row-scaled)
+  const float* sb;        // row-scaled B: 1x128 scales sb[kb * ld_sb + n]
+  int64_t ld_sb;
   void* y;              // grouped: direct stores (BF16 or FP32)
   int64_t ldy;
   int32_t M;            // rows of A (M_total when grouped)
@@ -88,14 +90,17 @@ struct Params {
   uint64_t timeout_ns;
 };
 
-template <int BN, int STAGES, int CG>
+template <int BN, int STAGES, int CG, bool RS = false>
 struct Smem {
   static constexpr int kA = BM * BK;
   static constexpr int kB = (BN / CG) * BK;  // this CTA's share of the B tile
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kA;
   static constexpr int kOffStaging = kOffB + STAGES * kB;
-  static constexpr int kOffBar = kOffStaging + kEpiWarps * kStagingBytes;
+  // row-scaled B: per promotion warp, two chunks x (BN / 2) column scales
+  static constexpr int kOffColScale = kOffStaging + kEpiWarps * kStagingBytes;
+  static constexpr int kColScaleBytes = RS ? kEpiWarps * 2 * (BN / 2) * 4 : 0;
+  static constexpr int kOffBar = kOffColScale + kColScaleBytes;
   // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2]
   static constexpr int kOffSlot = kOffBar + (2 * STAGES + 4) * 8;
   static constexpr int kOffAbort = kOffSlot + 4;
@@ -179,11 +184,12 @@ __device__ __forceinline__ void abort_cta(volatile int* abort_flag, unsigned* st
   record_status(status, kStatusTimeout);
 }
 
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS>
 __global__ void __launch_bounds__(kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using L = Smem<BN, STAGES, CG>;
+  using L = Smem<BN, STAGES, CG, RS>;
+  static_assert(!(RS && GROUPED), "row-scaled B is a dense-only variant");
   static_assert(CG == 1 || CG == 2, "single CTAs or CTA pairs");
   constexpr int kTmemCols = 2 * BN;   // two accumulator buffers of this CTA's 128 rows x BN
   constexpr int kHalfCols = BN / 2;   // columns per promotion warp
@@ -380,14 +386,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kHalfCols / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
+      // Row-scaled B: this warp's kHalfCols column scales per chunk, staged in
+      // a two-chunk shared-memory ring one chunk ahead (lane l fetches
+      // kColVec consecutive scales); every lane then reads all of them.
+      constexpr int kColVec = kHalfCols / 32;
+      float* colscale = reinterpret_cast<float*>(smem + L::kOffColScale) + epi * 2 * kHalfCols;
+      const float* sb_col = RS ? p.sb + col0 + lane * kColVec : nullptr;
+      float cs_next[kColVec];
+      if (RS) {
+#pragma unroll
+        for (int v = 0; v < kColVec; ++v) colscale[lane * kColVec + v] = __ldg(sb_col + v);
+        const int k1 = p.KB > 1 ? 1 : 0;
+#pragma unroll
+        for (int v = 0; v < kColVec; ++v) cs_next[v] = __ldg(sb_col + static_cast<int64_t>(k1) * p.ld_sb + v);
+        __syncwarp();
+      }
+
       float sa_next = __ldg(sa_col);
-      float sw_next = __ldg(sw_row);
+      float sw_next = RS ? 1.0f : __ldg(sw_row);
       for (int kb = 0; kb < p.KB; ++kb) {
         const float scale = sa_next * sw_next * row_mask;
         const float2 scale2 = make_float2(scale, scale);
         const int kn = kb + 1 < p.KB ? kb + 1 : kb;  // prefetch the next chunk's scales
         sa_next = __ldg(sa_col + static_cast<int64_t>(kn) * p.ld_sa);
-        sw_next = __ldg(sw_row + kn);
+        if (!RS) sw_next = __ldg(sw_row + kn);
+        const float* cs = colscale + (kb & 1) * kHalfCols;  // this chunk's column scales (RS)
         const bool waited = mbar_wait(bar_tfull + 8 * buf, bphase, abort_flag, p.timeout_ns);
         if (!__all_sync(0xffffffffu, waited)) {
           abort_cta(abort_flag, p.status);
@@ -413,11 +436,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_cluster_relaxed(tempty_base + 8 * buf);
             }
           }
+          if (!RS) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            acc[c * 32 + j] =
-                __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scale2,
-                           acc[c * 32 + j]);
+            for (int j = 0; j < 32; ++j)
+              acc[c * 32 + j] =
+                  __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), scale2,
+                             acc[c * 32 + j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float4 cs4 = *reinterpret_cast<const float4*>(cs + c * 64 + 2 * j);
+              const float2 s01 = __fmul2_rn(scale2, make_float2(cs4.x, cs4.y));
+              const float2 s23 = __fmul2_rn(scale2, make_float2(cs4.z, cs4.w));
+              acc[c * 32 + j] =
+                  __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), s01,
+                             acc[c * 32 + j]);
+              acc[c * 32 + j + 1] =
+                  __ffma2_rn(make_float2(__uint_as_float(r[2 * j + 2]), __uint_as_float(r[2 * j + 3])), s23,
+                             acc[c * 32 + j + 1]);
+            }
+          }
+        }
+        if (RS) {
+          // stage the next chunk's column scales (the slot was last read in
+          // chunk kb - 1) and fetch the one after
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < kColVec; ++v) colscale[((kb + 1) & 1) * kHalfCols + lane * kColVec + v] = cs_next[v];
+          const int k2 = kb + 2 < p.KB ? kb + 2 : p.KB - 1;
+#pragma unroll
+          for (int v = 0; v < kColVec; ++v) cs_next[v] = __ldg(sb_col + static_cast<int64_t>(k2) * p.ld_sb + v);
+          __syncwarp();
         }
         buf ^= 1u;
         if (buf == 0) bphase ^= 1u;
@@ -499,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Largest number of clusters of this kernel variant that can be resident at
 // once on the current device (queried once per device and variant).
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS>
 int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) {
   static std::atomic<int> cache[64];
   const int idx = dev.ordinal & 63;
@@ -508,7 +557,7 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
   n = dev.num_sms / CG;
   if (CG > 1) {
     int q = 0;
-    if (cudaOccupancyMaxActiveClusters(&q, blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32>, &cfg) == cudaSuccess &&
+    if (cudaOccupancyMaxActiveClusters(&q, blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS>, &cfg) == cudaSuccess &&
         q > 0)
       n = q;
     else
@@ -520,11 +569,11 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
 
 // Persistent launch: one cluster of CG CTAs per CG SMs, at most one per
 // cluster tile.
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS>
 cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                           const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream) {
-  using L = Smem<BN, STAGES, CG>;
-  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32>;
+  using L = Smem<BN, STAGES, CG, RS>;
+  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS>;
   if (BN == 256) {
     // setmaxnreg.inc only completes if the launch holds kRegsLaunch registers
     // per thread; refuse to launch a build that does not.
@@ -547,7 +596,7 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(CG, 1, 1);
-  const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32>(dev, cfg);
+  const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32, RS>(dev, cfg);
   const int64_t clusters = cluster_tiles < resident ? cluster_tiles : resident;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmY, p);
@@ -560,6 +609,13 @@ constexpr int kStagesPair = 6;   // BN = 256 on a CTA pair: 32 KB stages
 constexpr bool kUsePairs = true;
 constexpr int kStages256 = 4;    // BN = 256 on one CTA: 48 KB stages
 constexpr int kStages128 = 6;    // BN = 128 on one CTA: 32 KB stages
+// Row-scaled B stages its column scales in shared memory: one stage fewer.
+constexpr int kStagesPairRS = 5;
+constexpr int kStages256RS = 3;
+constexpr int kStages128RS = 5;
+static_assert(Smem<256, kStagesPairRS, 2, true>::kDynamic <= 232448, "shared memory budget (BN=256, pair, RS)");
+static_assert(Smem<256, kStages256RS, 1, true>::kDynamic <= 232448, "shared memory budget (BN=256, RS)");
+static_assert(Smem<128, kStages128RS, 1, true>::kDynamic <= 232448, "shared memory budget (BN=128, RS)");
 static_assert(Smem<256, kStagesPair, 2>::kDynamic <= 232448, "shared memory budget (BN=256, pair)");
 static_assert(Smem<256, kStages256, 1>::kDynamic <= 232448, "shared memory budget (BN=256)");
 static_assert(Smem<128, kStages128, 1>::kDynamic <= 232448, "shared memory budget (BN=128)");
@@ -570,6 +626,8 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
   p.sa = sa;
   p.ld_sa = ld_sa;
   p.sw = sw;
+  p.sb = nullptr;
+  p.ld_sb = 0;
   p.y = y;
   p.ldy = ldy;
   p.M = static_cast<int32_t>(M);
@@ -587,16 +645,19 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
 // pair (BN = 256 on a CTA pair, 256 x 256 per pair).
 enum class Shape { kNarrow, kWide, kPair };
 
-template <bool GROUPED, bool F32>
+template <bool GROUPED, bool F32, bool RS = false>
 cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream) {
   switch (shape) {
     case Shape::kNarrow:
-      return launch_kernel<128, kStages128, GROUPED, 1, F32>(dev, tmA, tmB, tmY, p, cluster_tiles, stream);
+      return launch_kernel<128, RS ? kStages128RS : kStages128, GROUPED, 1, F32, RS>(dev, tmA, tmB, tmY, p,
+                                                                                      cluster_tiles, stream);
     case Shape::kWide:
-      return launch_kernel<256, kStages256, GROUPED, 1, F32>(dev, tmA, tmB, tmY, p, cluster_tiles, stream);
+      return launch_kernel<256, RS ? kStages256RS : kStages256, GROUPED, 1, F32, RS>(dev, tmA, tmB, tmY, p,
+                                                                                      cluster_tiles, stream);
     case Shape::kPair:
-      return launch_kernel<256, kStagesPair, GROUPED, 2, F32>(dev, tmA, tmB, tmY, p, cluster_tiles, stream);
+      return launch_kernel<256, RS ? kStagesPairRS : kStagesPair, GROUPED, 2, F32, RS>(dev, tmA, tmB, tmY, p,
+                                                                                        cluster_tiles, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -646,6 +707,30 @@ cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, co
   const int64_t max_ctiles = (((M_total + BM - 1) / BM + G) / CG + G) * (N / BN);
   return y_f32 ? launch_shape<true, true>(shape, dev, tmA, tmB, tmY, p, max_ctiles, stream)
                : launch_shape<true, false>(shape, dev, tmA, tmB, tmY, p, max_ctiles, stream);
+}
+
+cudaError_t launch_blockscaled_gemm_rowscaled(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
+                                              int64_t ld_sa, const void* qb, int64_t ldqb, const float* sb,
+                                              int64_t ld_sb, void* y, int64_t ldy, bool y_f32, int64_t M, int64_t N,
+                                              int64_t K, cudaStream_t stream) {
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  const bool wide = (N % 256 == 0) && m_tiles * (N / 256) >= dev.num_sms;
+  const Shape shape = !wide ? Shape::kNarrow : (kUsePairs && m_tiles >= 2 ? Shape::kPair : Shape::kWide);
+  const int CG = shape == Shape::kPair ? 2 : 1;
+  const int BN = wide ? 256 : 128;
+  const int out_bytes = y_f32 ? 4 : 2;
+  CUtensorMap tmA, tmB, tmY;
+  if (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qb, K, N, ldqb, BK, BN / CG, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tmY, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M,
+                    ldy * out_bytes, kEpiRowBytes / out_bytes, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  Params p = make_params(dev, sa, ld_sa, nullptr, y, ldy, M, N, K, nullptr, 1);
+  p.sb = sb;
+  p.ld_sb = ld_sb;
+  const int64_t cluster_tiles = (m_tiles + CG - 1) / CG * (N / BN);
+  return y_f32 ? launch_shape<false, true, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream)
+               : launch_shape<false, false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream);
 }
 
 }  // namespace fp8bs

@@ -45,6 +45,21 @@ cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, co
 cudaError_t launch_dequant_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
                                           const float* sw, void* y, int64_t ldy, cudaStream_t stream);
 
+// Y = sum_kb sa[kb][m] * sb[kb][n] * chunk product (1x128 scales on both operands).
+cudaError_t launch_blockscaled_gemm_rowscaled(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
+                                              int64_t ld_sa, const void* qb, int64_t ldqb, const float* sb,
+                                              int64_t ld_sb, void* y, int64_t ldy, bool y_f32, int64_t M, int64_t N,
+                                              int64_t K, cudaStream_t stream);
+
+// 1x128 quantisation of X^T: codes [K, M] (row stride ldqt bytes), scales
+// st[m / 128][k] (row stride ld_st).  M % 128 == 0.
+cudaError_t launch_quant_act_1x128_t(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     void* qt, int64_t ldqt, float* st, int64_t ld_st, cudaStream_t stream);
+
+cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
+                                            const float* sw, void* qt, int64_t ldqt, float* swt,
+                                            cudaStream_t stream);
+
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace fp8bs

@@ -51,6 +51,16 @@ def dense_inputs(M, N, K, seed=0, w_std=0.02, outlier_frac=0.0, outlier_scale=1.
     return x.to(torch.bfloat16), w.to(torch.bfloat16)
 
 
+def backward_inputs(M, N, K, seed=0, w_std=0.02, dy_std=1.0):
+    """(x [M, K], w [N, K], dy [M, N]) BF16 CPU tensors for the backward GEMMs:
+    X and W drawn as in dense_inputs, then the output gradient dY ~ N(0, dy_std)."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(M, K, generator=g, dtype=torch.float32)
+    w = torch.randn(N, K, generator=g, dtype=torch.float32) * w_std
+    dy = torch.randn(M, N, generator=g, dtype=torch.float32) * dy_std
+    return x.to(torch.bfloat16), w.to(torch.bfloat16), dy.to(torch.bfloat16)
+
+
 def config_inputs(name: str, seed=0):
     """(x, w) for a dense configuration by name."""
     c = dict(CONFIGS[name])

@@ -151,6 +151,58 @@ fp8bs_status fp8_blockscaled_grouped_gemm_f32(int32_t G, const int32_t* group_of
 fp8bs_status fp8_dequant_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, const float* sw,
                                         void* y_bf16, int64_t ldy, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Backward GEMMs of the linear layer.  The excerpt keeps the activation in
+ * FP8 for the backward pass (paragraph 2) and splits the backward into its
+ * input-gradient and weight-gradient parts (paragraph 3):
+ *   dX = dY . W    : fp8_quant_act_1x128(dY) and fp8_transpose_weight_128x128
+ *                    of W's codes, then fp8_blockscaled_gemm;
+ *   dW = dY^T . X  : fp8_quant_act_1x128_t of dY and of X (1x128 tiles of the
+ *                    transposes: per channel per 128 tokens), then
+ *                    fp8_blockscaled_gemm_rowscaled(_f32).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * 1x128 quantisation of X^T for X [M, K] BF16 (row stride ldx): each run of
+ * 128 rows of one column is a group.
+ *   qt : [K, M] E4M3 codes of X^T out, row stride ldqt (bytes, % 16 == 0).
+ *   st : [M/128, ld_st] FP32 scales out, st[mb * ld_st + k] (ld_st >= K,
+ *        ld_st % 4 == 0) -- the activation-scale layout of X^T.
+ * M % 128 == 0 and K % 128 == 0 (FP8BS_ERR_UNSUPPORTED_SHAPE otherwise).
+ * Codes and scales equal fp8_quant_act_1x128 applied to X^T.
+ */
+fp8bs_status fp8_quant_act_1x128_t(const void* x_bf16, int64_t M, int64_t K, int64_t ldx,
+                                   void* qt, int64_t ldqt, float* st, int64_t ld_st, cudaStream_t stream);
+
+/*
+ * Codes and block scales of W^T from those of W [N, K]: a 128x128 block is
+ * a block either way round ("Figure 7 (a)" item (2)), so nothing is
+ * requantised.
+ *   qw  : [N, K] codes (row stride ldq);   sw  : [N/128, K/128] scales.
+ *   qwt : [K, N] codes out (row stride ldqt, % 16 == 0);
+ *   swt : [K/128, N/128] scales out, contiguous.
+ */
+fp8bs_status fp8_transpose_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, const float* sw,
+                                          void* qwt, int64_t ldqt, float* swt, cudaStream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM with 1x128 scales on BOTH operands (the weight-gradient
+ * GEMM, whose operands are quantised along the token dimension):
+ *   Y[m, n] = sum_kb sa[kb*ld_sa + m] * sb[kb*ld_sb + n]
+ *             * sum_{k in chunk kb} dec(qa[m, k]) * dec(qb[n, k]),
+ * promoted per 128-wide K chunk in FP32.  qa [M, K] (stride ldqa), qb [N, K]
+ * (stride ldqb), ld_sa >= M, ld_sb >= N, both % 4 == 0.  Y BF16 [M, N]
+ * (stride ldy), or FP32 for the _f32 variant (ldy % 4 == 0).
+ */
+fp8bs_status fp8_blockscaled_gemm_rowscaled(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                            const void* qb, int64_t ldqb, const float* sb, int64_t ld_sb,
+                                            void* y_bf16, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                            cudaStream_t stream);
+fp8bs_status fp8_blockscaled_gemm_rowscaled_f32(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                                const void* qb, int64_t ldqb, const float* sb, int64_t ld_sb,
+                                                float* y_f32, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                                cudaStream_t stream);
+
 /*
  * Text naming the CUDA error (and the step) behind the last FP8BS_ERR_CUDA
  * returned to the calling host thread; "" if none.  Valid until the thread's

@@ -7,6 +7,7 @@ from .fp8_oracle import (  # noqa: F401
     E4M3_MAX,
     GROUP,
     blockscaled_gemm,
+    blockscaled_gemm_rowscaled,
     blockscaled_grouped_gemm,
     bf16_round,
     dequant_weight_128x128,
@@ -14,7 +15,10 @@ from .fp8_oracle import (  # noqa: F401
     e4m3_decode,
     e4m3_encode_rne_satfinite,
     fl32_div,
+    linear_backward,
     linear_forward,
     quant_act_1x128,
+    quant_act_1x128_t,
     quant_weight_128x128,
+    transpose_weight_128x128,
 )

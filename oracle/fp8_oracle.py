@@ -254,6 +254,68 @@ def blockscaled_grouped_gemm(offsets, qa, sa, qw, sw):
     return y
 
 
+# ---------------------------------------------------------------------------
+# Backward GEMMs of the FP8 linear layer.
+#
+# The excerpt trains with the same FP8 GEMMs: the activation is cached in FP8
+# for the backward pass of the linear layer (paragraph 2) and the backward is
+# split into the input-gradient and weight-gradient parts (paragraph 3).
+#   dX = dY . W        : dY quantised 1x128 along N (its reduction dim), W's
+#                        128x128 blocks transposed (a block is a block either
+#                        way round, so the codes and scales just move);
+#   dW = dY^T . X      : the reduction runs over tokens, so both operands are
+#                        quantised 1x128 along M -- the 1x128 quantisation of
+#                        the transposed matrices -- and each chunk is promoted
+#                        with one scale per output row times one per column.
+# ---------------------------------------------------------------------------
+
+def quant_act_1x128_t(x):
+    """1x128 quantisation of x^T: for each column k of x [M, K] and each run
+    of 128 rows, one scale.  Returns codes [K, M] (x^T's layout) and scales
+    [M/128, K] (the activation-scale layout of x^T).  M % 128 == 0."""
+    x = np.asarray(x, dtype=np.float32)
+    return quant_act_1x128(np.ascontiguousarray(x.T))
+
+
+def transpose_weight_128x128(qw, sw):
+    """Codes and block scales of W^T from those of W: qw^T [K, N], sw^T
+    [K/128, N/128]."""
+    return np.ascontiguousarray(np.asarray(qw, dtype=np.uint8).T), np.ascontiguousarray(np.asarray(sw).T)
+
+
+def blockscaled_gemm_rowscaled(qa, sa, qb, sb):
+    """Y[m, n] = sum_kb sa[kb, m] * sb[kb, n] * (chunk kb of dec(qa) . dec(qb)^T)
+    with 1x128 scales on both operands (the weight-gradient GEMM).
+    qa uint8 [M, K], sa float32 [K/128, >=M], qb uint8 [N, K], sb float32
+    [K/128, >=N].  Returns float64 [M, N], unrounded."""
+    qa = np.asarray(qa, dtype=np.uint8)
+    qb = np.asarray(qb, dtype=np.uint8)
+    sa = np.asarray(sa, dtype=np.float32)
+    sb = np.asarray(sb, dtype=np.float32)
+    M, K = qa.shape
+    N = qb.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    for kb in range(K // GROUP):
+        cols = slice(kb * GROUP, (kb + 1) * GROUP)
+        chunk = e4m3_decode(qa[:, cols]) @ e4m3_decode(qb[:, cols]).T          # exact
+        y += chunk * (sa[kb, :M].astype(np.float64)[:, None] * sb[kb, :N].astype(np.float64)[None, :])
+    return y
+
+
+def linear_backward(x, w, dy):
+    """Both backward GEMMs on float32 inputs holding BF16 values:
+    dX = Q(dY) . Q(W)^T-blocks and dW = Q(dY^T) . Q(X^T)^T.
+    Returns (dx float64 [M, K], dw float64 [N, K])."""
+    qw, sw = quant_weight_128x128(w)
+    qdy, sdy = quant_act_1x128(dy)
+    qwt, swt = transpose_weight_128x128(qw, sw)
+    dx = blockscaled_gemm(qdy, sdy, qwt, swt)
+    qdyt, sdyt = quant_act_1x128_t(dy)
+    qxt, sxt = quant_act_1x128_t(x)
+    dw = blockscaled_gemm_rowscaled(qdyt, sdyt, qxt, sxt)
+    return dx, dw
+
+
 def linear_forward(x, w):
     """The whole hot path on float32 inputs holding BF16 values: quantise X
     per 1x128 tile and W per 128x128 block, then the block-scaled GEMM."""

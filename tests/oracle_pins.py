@@ -510,6 +510,114 @@ def pin_dequant_roundtrip(o):
     assert np.all(got == np.float32(1.1328125)), got[0, 0]
 
 
+# ---------------------------------------------------------------------------
+# Backward GEMMs
+# ---------------------------------------------------------------------------
+
+def pin_rowscaled_bruteforce(o):
+    """Exact rational sum on tiny inputs: element (m, n) gets
+    sa[kb, m] * sb[kb, n] times the exact chunk sum, per 128-wide chunk."""
+    rng = np.random.default_rng(43)
+    dec = [_frac_dec(c) for c in range(256)]
+    for M, N, K in ((3, 5, 128), (2, 4, 256)):
+        a = rng.standard_normal((M, K)).astype(np.float32)
+        b = (rng.standard_normal((N, K)) * 0.1).astype(np.float32)
+        qa, sa = o.quant_act_1x128(a)
+        qb, sb = o.quant_act_1x128(b)
+        y = o.blockscaled_gemm_rowscaled(qa, sa, qb, sb)
+        assert y.shape == (M, N)
+        for m in range(M):
+            for n in range(N):
+                tot, mag = Fraction(0), Fraction(0)
+                for kb in range(K // 128):
+                    part = sum(dec[int(qa[m, k])] * dec[int(qb[n, k])] for k in range(kb * 128, kb * 128 + 128))
+                    term = Fraction(float(sa[kb, m])) * Fraction(float(sb[kb, n])) * part
+                    tot += term
+                    mag += abs(term)
+                bound = 4 * (K // 128) * 2.0 ** -53 * float(mag)
+                assert abs(Fraction(float(y[m, n])) - tot) <= Fraction(bound), (M, N, K, m, n)
+
+
+def pin_rowscaled_reduces_to_blockscaled(o):
+    """With per-column scales that are constant over each 128-wide block of
+    output columns, the row-scaled product is the block-scaled one."""
+    rng = np.random.default_rng(47)
+    x = rng.standard_normal((7, 384)).astype(np.float32)
+    w = (rng.standard_normal((256, 384)) * 0.02).astype(np.float32)
+    qa, sa = o.quant_act_1x128(x)
+    qw, sw = o.quant_weight_128x128(w)
+    sb = np.repeat(sw.T, 128, axis=1)  # [K/128, N]: scale of column n in chunk kb = sw[n // 128, kb]
+    assert np.array_equal(o.blockscaled_gemm_rowscaled(qa, sa, qw, sb), o.blockscaled_gemm(qa, sa, qw, sw))
+
+
+def pin_transposed_quant_structure(o):
+    """1x128 tiles of x^T are runs of 128 rows of one column of x: constant
+    columns code to +-448 with s = fl32(|c| / 448); perturbing one element
+    changes only its own (row run, column) group."""
+    rng = np.random.default_rng(53)
+    c = (rng.standard_normal(6) * 4).astype(np.float32)
+    x = np.tile(c, (256, 1))
+    q, s = o.quant_act_1x128_t(x)
+    assert q.shape == (6, 256) and s.shape == (2, 6)
+    assert np.all((q == 0x7E) | (q == 0xFE))
+    assert np.array_equal(q == 0xFE, np.tile((c < 0)[:, None], (1, 256)))
+    for k in range(6):
+        want = _nearest_f32(Fraction(float(abs(c[k]))) / 448)
+        assert s[0, k] == want and s[1, k] == want
+    x = rng.standard_normal((256, 5)).astype(np.float32)
+    q0, s0 = o.quant_act_1x128_t(x)
+    x2 = x.copy()
+    x2[200, 3] = 100.0
+    q1, s1 = o.quant_act_1x128_t(x2)
+    assert {(k, m // 128) for k, m in zip(*np.nonzero(q0 != q1))} == {(3, 1)}
+    assert {(mb, k) for mb, k in zip(*np.nonzero(s0 != s1))} == {(1, 3)}
+
+
+def pin_backward_error_bound(o):
+    """dX and dW stay within the worst case that E4M3 rounding allows of the
+    unquantised float64 products dY . W and dY^T . X (half an E4M3 ulp per
+    operand: 2^-4 relative in the normal range, 2^-10 * s below it); a
+    transposed or mis-scaled operand breaks the bound by orders of
+    magnitude."""
+    rng = np.random.default_rng(59)
+    M, N, K = 256, 256, 384
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    dy = (rng.standard_normal((M, N)) * 0.5).astype(np.float32)
+    dx, dw = o.linear_backward(x, w, dy)
+
+    def err(v, s):
+        return np.maximum(np.abs(v) * 2.0 ** -4, s * 2.0 ** -10)
+
+    # dX = dY . W: dY groups 1x128 along N, W blocks 128x128
+    _, sdy = o.quant_act_1x128(dy)
+    _, sw = o.quant_weight_128x128(w)
+    e_dy = err(dy.astype(np.float64), np.repeat(sdy.T.astype(np.float64), 128, axis=1))
+    e_w = err(w.astype(np.float64), np.repeat(np.repeat(sw.astype(np.float64), 128, 0), 128, 1))
+    ad, aw = np.abs(dy.astype(np.float64)), np.abs(w.astype(np.float64))
+    bound = ad @ e_w + e_dy @ aw + e_dy @ e_w
+    assert np.all(np.abs(dx - dy.astype(np.float64) @ w.astype(np.float64)) <= bound * (1 + 1e-9) + 1e-30)
+    # dW = dY^T . X: both grouped along M
+    _, sdyt = o.quant_act_1x128_t(dy)
+    _, sxt = o.quant_act_1x128_t(x)
+    e_dyt = err(dy.T.astype(np.float64), np.repeat(sdyt.T.astype(np.float64), 128, axis=1))
+    e_xt = err(x.T.astype(np.float64), np.repeat(sxt.T.astype(np.float64), 128, axis=1))
+    adt, axt = np.abs(dy.T.astype(np.float64)), np.abs(x.T.astype(np.float64))
+    bound = adt @ e_xt.T + e_dyt @ axt.T + e_dyt @ e_xt.T
+    assert np.all(np.abs(dw - dy.T.astype(np.float64) @ x.astype(np.float64)) <= bound * (1 + 1e-9) + 1e-30)
+
+
+def pin_backward_linearity(o):
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((128, 256)).astype(np.float32)
+    w = (rng.standard_normal((128, 256)) * 0.02).astype(np.float32)
+    dy = rng.standard_normal((128, 128)).astype(np.float32)
+    dx0, dw0 = o.linear_backward(x, w, dy)
+    for j in (-6, 5):
+        dx1, dw1 = o.linear_backward(x, w, (dy * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(dx1, dx0 * 2.0 ** j) and np.array_equal(dw1, dw0 * 2.0 ** j)
+
+
 ALL_PINS = [
     pin_codec_format_points,
     pin_codec_roundtrip,
@@ -534,4 +642,9 @@ ALL_PINS = [
     pin_grouped,
     pin_bf16_round,
     pin_dequant_roundtrip,
+    pin_rowscaled_bruteforce,
+    pin_rowscaled_reduces_to_blockscaled,
+    pin_transposed_quant_structure,
+    pin_backward_error_bound,
+    pin_backward_linearity,
 ]

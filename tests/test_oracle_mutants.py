@@ -78,6 +78,21 @@ MUTANTS = {
     "dequant_scale_of_first_block": (
         "scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float32), GROUP, axis=0), GROUP, axis=1)",
         "scale = np.full(qw.shape, np.asarray(sw, dtype=np.float32).flat[0], dtype=np.float32)"),
+    "rowscaled_column_scale_of_chunk_0": (
+        "y += chunk * (sa[kb, :M].astype(np.float64)[:, None] * sb[kb, :N].astype(np.float64)[None, :])",
+        "y += chunk * (sa[kb, :M].astype(np.float64)[:, None] * sb[0, :N].astype(np.float64)[None, :])"),
+    "rowscaled_column_scale_dropped": (
+        "y += chunk * (sa[kb, :M].astype(np.float64)[:, None] * sb[kb, :N].astype(np.float64)[None, :])",
+        "y += chunk * (sa[kb, :M].astype(np.float64)[:, None] + 0 * sb[kb, :N].astype(np.float64)[None, :])"),
+    "backward_weight_not_transposed": (
+        "dx = blockscaled_gemm(qdy, sdy, qwt, swt)",
+        "dx = blockscaled_gemm(qdy, sdy, qw, sw)"),
+    "backward_wgrad_operands_swapped": (
+        "dw = blockscaled_gemm_rowscaled(qdyt, sdyt, qxt, sxt)",
+        "dw = blockscaled_gemm_rowscaled(qdyt, sdyt, qdyt, sdyt)"),
+    "transposed_quant_not_transposed": (
+        "return quant_act_1x128(np.ascontiguousarray(x.T))",
+        "return quant_act_1x128(x)"),
     "grouped_wrong_weight_scales": (
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])",
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[0])"),
