@@ -18,6 +18,11 @@ _API = (
     "fp8_transpose_weight_128x128",
     "fp8_blockscaled_gemm_rowscaled",
     "linear_backward",
+    "fp8_quant_per_token",
+    "fp8_quant_per_channel",
+    "e5m6_encode",
+    "e5m6_decode",
+    "fp8_swiglu_quant_act_1x128",
     "fp8bs_last_device_error",
     "fp8bs_set_wait_timeout_ns",
     "fp8bs_selftest_wait_timeout",

@@ -36,6 +36,11 @@ EXPORTS = {
     "fp8_blockscaled_grouped_gemm_f32": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
     "fp8_dequant_weight_128x128": [_p, _i64, _i64, _i64, _p, _p, _i64, _p],
     "fp8_quant_act_1x128_t": [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
+    "fp8_quant_per_token": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
+    "fp8_quant_per_channel": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
+    "fp8bs_e5m6_encode_bf16": [_p, _i64, _p, _p],
+    "fp8bs_e5m6_decode_bf16": [_p, _i64, _p, _p],
+    "fp8_swiglu_quant_act_1x128": [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p, _i64, _p],
     "fp8_transpose_weight_128x128": [_p, _i64, _i64, _i64, _p, _p, _i64, _p, _p],
     "fp8_blockscaled_gemm_rowscaled": [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_gemm_rowscaled_f32": [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64,
@@ -255,6 +260,67 @@ def fp8_blockscaled_gemm_rowscaled(qa, sa, qb, sb, y=None, stream=None, out_dtyp
                               sb.stride(0), _ptr(y), y.stride(0), M, N, K, _stream(stream))
     _check(fn, status)
     return y
+
+
+def fp8_quant_per_token(x, q=None, s=None, stream=None):
+    """x bf16 [M, K] -> (q uint8 [M, K], s float32 [M]): one scale per row."""
+    _require(x, torch.bfloat16, "x", 2)
+    M, K = x.shape
+    q = q if q is not None else torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = s if s is not None else torch.empty((M,), dtype=torch.float32, device=x.device)
+    _require(q, torch.uint8, "q", 2)
+    st = lib.fp8_quant_per_token(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), _stream(stream))
+    _check("fp8_quant_per_token", st)
+    return q, s
+
+
+def fp8_quant_per_channel(x, q=None, s=None, stream=None):
+    """x bf16 [M, K] -> (q uint8 [M, K], s float32 [K]): one scale per column."""
+    _require(x, torch.bfloat16, "x", 2)
+    M, K = x.shape
+    q = q if q is not None else torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = s if s is not None else torch.empty((K,), dtype=torch.float32, device=x.device)
+    _require(q, torch.uint8, "q", 2)
+    st = lib.fp8_quant_per_channel(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), _stream(stream))
+    _check("fp8_quant_per_channel", st)
+    return q, s
+
+
+def e5m6_encode(x, codes=None, stream=None):
+    """BF16 tensor (any shape, contiguous) -> E5M6 codes as int16 of the same shape."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or not x.is_cuda:
+        raise TypeError("x must be a contiguous CUDA bfloat16 tensor")
+    codes = codes if codes is not None else torch.empty(x.shape, dtype=torch.int16, device=x.device)
+    st = lib.fp8bs_e5m6_encode_bf16(_ptr(x), x.numel(), _ptr(codes), _stream(stream))
+    _check("fp8bs_e5m6_encode_bf16", st)
+    return codes
+
+
+def e5m6_decode(codes, y=None, stream=None):
+    """E5M6 codes (int16, contiguous) -> BF16 values of the same shape (exact)."""
+    if codes.dtype != torch.int16 or not codes.is_contiguous() or not codes.is_cuda:
+        raise TypeError("codes must be a contiguous CUDA int16 tensor")
+    y = y if y is not None else torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
+    st = lib.fp8bs_e5m6_decode_bf16(_ptr(codes), codes.numel(), _ptr(y), _stream(stream))
+    _check("fp8bs_e5m6_decode_bf16", st)
+    return y
+
+
+def fp8_swiglu_quant_act_1x128(gate_up, qa=None, sa=None, h=None, return_h=False, stream=None):
+    """gate_up bf16 [M, 2F] (gate | up) -> (qa uint8 [M, F], sa float32 [F/128, ld_sa]) of
+    h = bf16(silu(gate) * up); with return_h, also h (bf16 [M, F])."""
+    _require(gate_up, torch.bfloat16, "gate_up", 2)
+    M, F2 = gate_up.shape
+    F = F2 // 2
+    qa = qa if qa is not None else torch.empty((M, F), dtype=torch.uint8, device=gate_up.device)
+    sa = sa if sa is not None else torch.empty((F // 128, ld_sa_for(M)), dtype=torch.float32, device=gate_up.device)
+    if return_h and h is None:
+        h = torch.empty((M, F), dtype=torch.bfloat16, device=gate_up.device)
+    st = lib.fp8_swiglu_quant_act_1x128(_ptr(gate_up), M, F, gate_up.stride(0), _ptr(qa), qa.stride(0), _ptr(sa),
+                                        sa.stride(0), _ptr(h), h.stride(0) if h is not None else 0,
+                                        _stream(stream))
+    _check("fp8_swiglu_quant_act_1x128", st)
+    return (qa, sa, h) if return_h else (qa, sa)
 
 
 def linear_backward(x, w, dy, stream=None, grad_dtype=torch.float32):

@@ -310,6 +310,83 @@ fp8bs_status fp8_transpose_weight_128x128(const void* qw, int64_t N, int64_t K, 
   return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_transpose_weight_128x128 launch", e);
 }
 
+fp8bs_status fp8_quant_per_token(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                                 float* s, cudaStream_t stream) {
+  if (M < 0 || K < 0 || ldx < 0 || ldq < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 8 != 0 || K > 32768 || M > kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K || ldq < K) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (x_bf16 == nullptr || q == nullptr || s == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(q) || (reinterpret_cast<uintptr_t>(s) & 3u) != 0 || ldx % 8 != 0 ||
+      ldq % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_quant_per_token(*dev, x_bf16, M, K, ldx, q, ldq, s, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_per_token launch", e);
+}
+
+fp8bs_status fp8_quant_per_channel(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                                   float* s, cudaStream_t stream) {
+  if (M < 0 || K < 0 || ldx < 0 || ldq < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 8 != 0 || K > kMaxDim || M > kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldx < K || ldq < K) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (x_bf16 == nullptr || q == nullptr || s == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(s) || ldx % 8 != 0 || ldq % 16 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_quant_per_channel(*dev, x_bf16, M, K, ldx, q, ldq, s, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_per_channel launch", e);
+}
+
+fp8bs_status fp8bs_e5m6_encode_bf16(const void* x_bf16, int64_t n, void* codes, cudaStream_t stream) {
+  if (n < 0) return FP8BS_ERR_INVALID_ARG;
+  if (n % 8 != 0 || n > (int64_t{1} << 40)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return FP8BS_OK;
+  if (x_bf16 == nullptr || codes == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(codes)) return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_cast_e5m6(*dev, x_bf16, n, codes, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8bs_e5m6_encode_bf16 launch", e);
+}
+
+fp8bs_status fp8bs_e5m6_decode_bf16(const void* codes, int64_t n, void* y_bf16, cudaStream_t stream) {
+  if (n < 0) return FP8BS_ERR_INVALID_ARG;
+  if (n % 8 != 0 || n > (int64_t{1} << 40)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return FP8BS_OK;
+  if (codes == nullptr || y_bf16 == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(y_bf16)) return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_e5m6_to_bf16(*dev, codes, n, y_bf16, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8bs_e5m6_decode_bf16 launch", e);
+}
+
+fp8bs_status fp8_swiglu_quant_act_1x128(const void* gate_up_bf16, int64_t M, int64_t F, int64_t ld, void* qa,
+                                        int64_t ldq, float* sa, int64_t ld_sa, void* h_bf16, int64_t ldh,
+                                        cudaStream_t stream) {
+  if (M < 0 || F < 0 || ld < 0 || ldq < 0 || ld_sa < 0 || ldh < 0) return FP8BS_ERR_INVALID_ARG;
+  if (F == 0 || F % 128 != 0 || F > kMaxDim / 2 || M > kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ld < 2 * F || ldq < F || ld_sa < M || (h_bf16 != nullptr && ldh < F)) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (gate_up_bf16 == nullptr || qa == nullptr || sa == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(gate_up_bf16) || !aligned16(qa) || !aligned16(sa) || ld % 8 != 0 || ldq % 16 != 0 ||
+      ld_sa % 4 != 0 || (h_bf16 != nullptr && (!aligned16(h_bf16) || ldh % 8 != 0)))
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_swiglu_quant_act_1x128(*dev, gate_up_bf16, M, F, ld, qa, ldq, sa, ld_sa, h_bf16, ldh, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_swiglu_quant_act_1x128 launch", e);
+}
+
 fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,
                                   int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,
                                   int64_t K, cudaStream_t stream) {

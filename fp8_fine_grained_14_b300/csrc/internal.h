@@ -60,6 +60,17 @@ cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q
                                             const float* sw, void* qt, int64_t ldqt, float* swt,
                                             cudaStream_t stream);
 
+// Quantisation variants (variants.cu).
+cudaError_t launch_quant_per_token(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx, void* q,
+                                   int64_t ldq, float* s, cudaStream_t stream);
+cudaError_t launch_quant_per_channel(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     void* q, int64_t ldq, float* s, cudaStream_t stream);
+cudaError_t launch_cast_e5m6(const DeviceInfo& dev, const void* x, int64_t n, void* codes, cudaStream_t stream);
+cudaError_t launch_e5m6_to_bf16(const DeviceInfo& dev, const void* codes, int64_t n, void* y, cudaStream_t stream);
+cudaError_t launch_swiglu_quant_act_1x128(const DeviceInfo& dev, const void* gate_up, int64_t M, int64_t F,
+                                          int64_t ld, void* q, int64_t ldq, float* sa, int64_t ld_sa, void* h,
+                                          int64_t ldh, cudaStream_t stream);
+
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
 
 }  // namespace fp8bs

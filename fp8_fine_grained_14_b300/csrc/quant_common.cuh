@@ -42,11 +42,12 @@ __device__ __forceinline__ float rcp_approx(float s) {
 // 2^-19), rounded.  With every rounding counted, x * r_lo < fl32(x / s) <
 // x * r_hi for x > 0 (reversed for x < 0) with a margin of more than 2^-21
 // relative.  E4M3 rounding with saturation is monotonic, so when both ends
-// give the same code the quotient gives it too.  Only pairs whose bracket
-// straddles a rounding boundary (about 2^-14 of random data) are recomputed
-// with the IEEE division.  Products that underflow keep the sign of x and
-// code to +-0 at both ends, as the quotient does.  Subnormal scales, whose
-// reciprocal may overflow, take the division for the whole group.
+// give the same code the quotient gives it too.  Elements whose bracket holds
+// a rounding boundary -- for BF16 data about 0.5 %, almost all exact E4M3
+// ties, since BF16 values and their group scale are short binary numbers --
+// are decided exactly by straddle_code.  Products that underflow keep the sign
+// of x and code to +-0 at both ends, as the quotient does.  Subnormal scales,
+// whose reciprocal may overflow, take the IEEE division for the whole group.
 struct GroupScale {
   float s;
   float2 r_lo;
@@ -94,6 +95,78 @@ static __device__ __noinline__ uint2 quantise8_div(uint4 v, float s) {
   return make_uint2(cvt_e4m3x4(f[0], f[1], f[2], f[3]), cvt_e4m3x4(f[4], f[5], f[6], f[7]));
 }
 
+// Magnitude of an E4M3 code 0x00 .. 0x7E as a float32 (exact).
+__device__ __forceinline__ float e4m3_magnitude(uint32_t m) {
+  const uint32_t e = m >> 3, f = m & 7u;
+  return e == 0 ? static_cast<float>(f) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (f << 20));
+}
+
+// Exact code of one element whose bracketing products fell on different
+// codes m_lo < m_hi (magnitudes; the bracket holds the rounding boundary mu,
+// their midpoint).  fl32(x / s) is above mu, equal to it, or below it as
+// x / s lies above mu + h+, inside [mu - h-, mu + h+], or below mu - h-, with
+// h+- half a float32 ulp of mu above / below (ties of the float32 rounding go
+// to mu, whose significand is even).  The comparisons are done exactly in
+// 64-bit integers: |x| = X 2^a (X <= 8 bits, BF16), s = S 2^b (S 24 bits),
+// mu +- h = T 2^u with u = e(mu) - 25 (T < 2^26), so |x| > (mu + h+) s is
+// X 2^(a - u - b) > T S, a comparison of numbers below 2^56.  For BF16 inputs
+// these elements are nearly all exact E4M3 ties, which take the even code.
+// Anything outside the expected magnitudes falls back to the IEEE division.
+static __device__ __noinline__ uint32_t straddle_code(float x, uint32_t c_lo, uint32_t c_hi, float s) {
+  const uint32_t m_lo = c_lo & 0x7Fu, m_hi = c_hi & 0x7Fu;
+  const uint32_t sign = (__float_as_uint(x) >> 31) << 7;
+  const uint32_t xa = __float_as_uint(x) & 0x7FFFFFFFu;
+  const uint32_t sb = __float_as_uint(s);
+  const float mu = 0.5f * (e4m3_magnitude(m_lo) + e4m3_magnitude(m_hi));
+  const uint32_t mb = __float_as_uint(mu);
+  // |x| = X 2^a
+  const int xe = static_cast<int>(xa >> 23);
+  const uint64_t X = xe ? ((xa & 0x7FFFFFu) | 0x800000u) >> 16 : (xa & 0x7FFFFFu) >> 16;
+  const int a = (xe ? xe : 1) - 127 - 7;
+  // s = S 2^b (normal: the caller guarantees it)
+  const uint64_t S = (sb & 0x7FFFFFu) | 0x800000u;
+  const int b = static_cast<int>((sb >> 23) & 0xFFu) - 150;
+  // mu = P 2^u, u = e(mu) - 25, P in [2^25, 2^26)
+  const int mexp = static_cast<int>((mb >> 23) & 0xFFu) - 127;
+  const uint64_t P = static_cast<uint64_t>((mb & 0x7FFFFFu) | 0x800000u) << 2;
+  const int u = mexp - 25;
+  const bool pow2 = (mb & 0x7FFFFFu) == 0u;
+  const int shift = a - u - b;
+  if (m_hi != m_lo + 1u || m_hi > 0x7Eu || xa == 0u || shift < 0 || shift > 63 - 8) {
+    uint32_t code;
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(code)
+        : "f"(__fdiv_rn(x, s)));
+    return code & 0xFFu;
+  }
+  const uint64_t lhs = X << shift;
+  const uint64_t upper = (P + 2u) * S;               // (mu + h+) s in units of 2^(u + b)
+  const uint64_t lower = (P - (pow2 ? 1u : 2u)) * S;  // (mu - h-) s
+  uint32_t m;
+  if (lhs > upper)
+    m = m_hi;
+  else if (lhs < lower)
+    m = m_lo;
+  else
+    m = (m_lo & 1u) ? m_hi : m_lo;  // fl32(x / s) == mu: E4M3 tie, even code
+  return m | sign;
+}
+
+// Replace the codes of the straddling elements (bytes where lo and hi
+// differ) of one 4-element word by the code of the IEEE quotient.
+__device__ __forceinline__ uint32_t fix_word(uint32_t lo, uint32_t hi, uint32_t w0, uint32_t w1, float s) {
+  uint32_t diff = lo ^ hi;
+  while (diff != 0u) {
+    const int byte = (__ffs(diff) - 1) >> 3;
+    const uint32_t word = byte < 2 ? w0 : w1;
+    const float x = (byte & 1) ? bf16hi_to_f32(word) : bf16lo_to_f32(word);
+    const uint32_t code = cvt_e4m3x4(__fdiv_rn(x, s), 0.0f, 0.0f, 0.0f) & 0xFFu;
+    lo = (lo & ~(0xFFu << (8 * byte))) | (code << (8 * byte));
+    diff &= ~(0xFFu << (8 * byte));
+  }
+  return lo;
+}
+
 // Quantise 8 BF16 values (one 16-byte vector) of a group into 8 codes.
 __device__ __forceinline__ uint2 quantise8(const uint4 v, const GroupScale& g) {
   if (g.s == 0.0f) return make_uint2(0u, 0u);  // all-zero group
@@ -103,10 +176,32 @@ __device__ __forceinline__ uint2 quantise8(const uint4 v, const GroupScale& g) {
   const float2 bl = __fmul2_rn(b, g.r_lo), bh = __fmul2_rn(b, g.r_hi);
   const float2 cl = __fmul2_rn(c, g.r_lo), ch = __fmul2_rn(c, g.r_hi);
   const float2 dl = __fmul2_rn(d, g.r_lo), dh = __fmul2_rn(d, g.r_hi);
-  const uint32_t lo0 = cvt_e4m3x4(al.x, al.y, bl.x, bl.y), hi0 = cvt_e4m3x4(ah.x, ah.y, bh.x, bh.y);
-  const uint32_t lo1 = cvt_e4m3x4(cl.x, cl.y, dl.x, dl.y), hi1 = cvt_e4m3x4(ch.x, ch.y, dh.x, dh.y);
-  if (lo0 == hi0 && lo1 == hi1 && g.bracket_ok) return make_uint2(lo0, lo1);
-  return quantise8_div(v, g.s);
+  uint32_t lo0 = cvt_e4m3x4(al.x, al.y, bl.x, bl.y);
+  const uint32_t hi0 = cvt_e4m3x4(ah.x, ah.y, bh.x, bh.y);
+  uint32_t lo1 = cvt_e4m3x4(cl.x, cl.y, dl.x, dl.y);
+  const uint32_t hi1 = cvt_e4m3x4(ch.x, ch.y, dh.x, dh.y);
+  if (!g.bracket_ok) return quantise8_div(v, g.s);
+  if (((lo0 ^ hi0) | (lo1 ^ hi1)) != 0u) {
+    lo0 = fix_word(lo0, hi0, v.x, v.y, g.s);
+    lo1 = fix_word(lo1, hi1, v.z, v.w, g.s);
+  }
+  return make_uint2(lo0, lo1);
+}
+
+// Code of a single value with its own group's scale (the per-element form of
+// quantise8, for groups that run across vectors).
+__device__ __forceinline__ uint32_t quantise1(float x, const GroupScale& g) {
+  if (g.s == 0.0f) return 0u;
+  if (!g.bracket_ok) {
+    uint32_t code;
+    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+        : "=r"(code)
+        : "f"(__fdiv_rn(x, g.s)));
+    return code & 0xFFu;
+  }
+  const uint32_t lo = cvt_e4m3x4(__fmul_rn(x, g.r_lo.x), 0.0f, 0.0f, 0.0f) & 0xFFu;
+  const uint32_t hi = cvt_e4m3x4(__fmul_rn(x, g.r_hi.x), 0.0f, 0.0f, 0.0f) & 0xFFu;
+  return lo == hi ? lo : straddle_code(x, lo, hi, g.s);
 }
 
 __device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {

@@ -1,0 +1,339 @@
+// variants.cu — quantisation variants for sm_103a: FP8 per token and per
+// channel, the E5M6 activation format, and SwiGLU fused with the 1x128
+// quantiser.
+//
+// Method: the TileKernels release ("DeepSeek starts updating frequently",
+// the tile kernels' features, item "Quantification") converts to FP8 / FP4 /
+// E5M6 per token, per block and per channel and fuses SwiGLU with the
+// quantisation; the V3 excerpt ("The Definitive Information To Deepseek",
+// paragraph 3) keeps certain activations in a custom E5M6 format.  Every FP8
+// variant uses the same exact group quantiser as the 1x128 / 128x128 kernels
+// (quant_common.cuh): s = fl32(amax / 448), codes E4M3_RNE_satfinite(x / s).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant_common.cuh"
+
+namespace fp8bs {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Per token: one CTA (256 threads) per row, the row held in registers (U
+// 16-byte vectors per thread, K <= 2048 U), amax reduced across the CTA.
+// ---------------------------------------------------------------------------
+template <int U>
+__global__ void __launch_bounds__(256) quant_per_token_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
+                                                              int64_t ldx_v, uint2* __restrict__ q, int64_t ldq_v,
+                                                              float* __restrict__ s) {
+  __shared__ uint32_t warp_max[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const uint4* src = x + row * ldx_v;
+    uint4 v[U];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = threadIdx.x + 256 * u;
+      v[u] = i < KV ? ld_nc_v4(src + i) : make_uint4(0u, 0u, 0u, 0u);
+      m = max_pairs(m, absmax8_pairs(v[u]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) warp_max[warp] = m;
+    __syncthreads();
+    m = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = max_pairs(m, warp_max[i]);
+    __syncthreads();  // warp_max is reused by the next row
+    const GroupScale g = group_scale(pairs_to_max(m));
+    if (threadIdx.x == 0) s[row] = g.s;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = threadIdx.x + 256 * u;
+      if (i < KV) q[row * ldq_v + i] = quantise8(v[u], g);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per channel: (1) column maxima of |x| as BF16 bit patterns (non-negative
+// values order like their patterns), reduced across a CTA in shared memory
+// and merged into s with atomicMax, (2) every element quantised with its
+// column's scale, (3) s turned from maxima into scales.  A CTA covers 256
+// columns (thread t: the 8 columns of vector t % 32) and walks row tiles of 64
+// (thread t: rows t / 32 + 8 i).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) channel_absmax_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
+                                                             int64_t ldx_v, uint32_t* __restrict__ amax_bits) {
+  __shared__ uint32_t part[8][32 * 4];  // [row slot][packed column pairs]
+  const int lane = threadIdx.x & 31, r8 = threadIdx.x >> 5;
+  const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  const int64_t row_tiles = (M + 63) / 64;
+  uint32_t mm[4] = {0u, 0u, 0u, 0u};
+  if (col_v < KV) {
+    for (int64_t tile = blockIdx.y; tile < row_tiles; tile += gridDim.y) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t row = tile * 64 + r8 + 8 * i;
+        if (row < M) {
+          const uint4 v = ld_nc_v4(x + row * ldx_v + col_v);
+          constexpr uint32_t kMag = 0x7FFF7FFFu;
+          mm[0] = max_pairs(mm[0], v.x & kMag);
+          mm[1] = max_pairs(mm[1], v.y & kMag);
+          mm[2] = max_pairs(mm[2], v.z & kMag);
+          mm[3] = max_pairs(mm[3], v.w & kMag);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) part[r8][lane * 4 + i] = mm[i];
+  __syncthreads();
+  if (r8 == 0 && col_v < KV) {
+    uint32_t* dst = amax_bits + col_v * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t m = part[0][lane * 4 + i];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) m = max_pairs(m, part[k][lane * 4 + i]);
+      atomicMax(dst + 2 * i, m & 0xFFFFu);
+      atomicMax(dst + 2 * i + 1, m >> 16);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) quant_per_channel_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
+                                                                int64_t ldx_v, const uint32_t* __restrict__ amax_bits,
+                                                                uint2* __restrict__ q, int64_t ldq_v) {
+  const int lane = threadIdx.x & 31, r8 = threadIdx.x >> 5;
+  const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+  if (col_v >= KV) return;
+  GroupScale g[8];  // the scales of this thread's 8 columns
+#pragma unroll
+  for (int c = 0; c < 8; ++c) g[c] = group_scale(__uint_as_float(__ldg(amax_bits + col_v * 8 + c) << 16));
+  const int64_t row_tiles = (M + 63) / 64;
+  for (int64_t tile = blockIdx.y; tile < row_tiles; tile += gridDim.y) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t row = tile * 64 + r8 + 8 * i;
+      if (row < M) {
+        const uint4 v = ld_nc_v4(x + row * ldx_v + col_v);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[2] = {0u, 0u};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float xv = (c & 1) ? bf16hi_to_f32(w[c >> 1]) : bf16lo_to_f32(w[c >> 1]);
+          out[c >> 2] |= quantise1(xv, g[c]) << (8 * (c & 3));
+        }
+        q[row * ldq_v + col_v] = make_uint2(out[0], out[1]);
+      }
+    }
+  }
+}
+
+__global__ void channel_scales_kernel(uint32_t* __restrict__ amax_bits_to_scales, int64_t K) {
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (k < K) {
+    const float amax = __uint_as_float(amax_bits_to_scales[k] << 16);
+    amax_bits_to_scales[k] = __float_as_uint(group_scale(amax).s);
+  }
+}
+
+__global__ void zero_words_kernel(uint32_t* __restrict__ p, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// E5M6: sign, 5 exponent bits (bias 15), 6 mantissa bits in the low 12 bits
+// of a 16-bit word; subnormals 2^-14 * m / 64; round to nearest even,
+// magnitudes above 65024 saturate (no scale).  Encoding rounds the float32
+// bit pattern directly: adding 0xFFFF plus the kept LSB to the pattern and
+// dropping 17 bits rounds the significand to 6 bits with ties to even and
+// carries into the exponent; re-biasing 127 -> 15 gives the code.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e5m6_encode(float f) {
+  const uint32_t bits = __float_as_uint(f);
+  const uint32_t sign = (bits >> 31) << 11;
+  const uint32_t a = bits & 0x7FFFFFFFu;
+  uint32_t code;
+  if (a > 0x477E0000u) {                 // |f| > 65024
+    code = 0x7BFu;
+  } else if (a >= 0x38800000u) {         // |f| >= 2^-14: normal E5M6
+    code = ((a + 0xFFFFu + ((a >> 17) & 1u)) >> 17) - (112u << 6);
+  } else {                               // subnormal E5M6: multiples of 2^-20
+    code = __float2uint_rn(__uint_as_float(a) * 0x1p20f);
+  }
+  return code | sign;
+}
+
+__device__ __forceinline__ uint32_t e5m6_to_bf16(uint32_t c) {
+  const uint32_t sign = (c & 0x800u) << 4;
+  const uint32_t e = (c >> 6) & 0x1Fu, m = c & 0x3Fu;
+  uint32_t f;
+  if (e == 0)
+    f = __float_as_uint(static_cast<float>(m) * 0x1p-20f);
+  else if (e == 31)
+    f = m == 0 ? 0x7F800000u : 0x7FC00000u;
+  else
+    f = ((e + 112u) << 23) | (m << 17);
+  return sign | (f >> 16);  // exact: the low 16 bits are zero
+}
+
+__global__ void __launch_bounds__(256) cast_e5m6_kernel(const uint4* __restrict__ x, int64_t nv,
+                                                        uint4* __restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < nv;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const uint4 v = ld_nc_v4(x + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = e5m6_encode(bf16lo_to_f32(w[k])) | (e5m6_encode(bf16hi_to_f32(w[k])) << 16);
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+__global__ void __launch_bounds__(256) e5m6_to_bf16_kernel(const uint4* __restrict__ c, int64_t nv,
+                                                           uint4* __restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < nv;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const uint4 v = ld_nc_v4(c + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = e5m6_to_bf16(w[k] & 0xFFFFu) | (e5m6_to_bf16(w[k] >> 16) << 16);
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU + 1x128 quantisation: h = bf16(silu(g) * u), silu(g) = g / (1 +
+// exp(-g)) in float32 (expf and the IEEE division), then the 1x128 quantiser
+// on the BF16 h.  Layout and tiling as the activation quantiser: grid x over
+// pairs of 128-channel groups of h, y over 16-row tiles; half-warp per row.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t swiglu_pair(uint32_t g2, uint32_t u2) {
+  const float g0 = bf16lo_to_f32(g2), g1 = bf16hi_to_f32(g2);
+  const float u0 = bf16lo_to_f32(u2), u1 = bf16hi_to_f32(u2);
+  const float h0 = __fmul_rn(__fdiv_rn(g0, __fadd_rn(1.0f, expf(-g0))), u0);
+  const float h1 = __fmul_rn(__fdiv_rn(g1, __fadd_rn(1.0f, expf(-g1))), u1);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+template <int U>
+__global__ void __launch_bounds__(256) swiglu_quant_kernel(const uint4* __restrict__ gu, int64_t M, int64_t FB,
+                                                           int64_t ld_v, uint2* __restrict__ q, int64_t ldq_v,
+                                                           float* __restrict__ sa, int64_t ld_sa,
+                                                           uint4* __restrict__ h_out, int64_t ldh_v) {
+  const int lane16 = threadIdx.x & 15;
+  const int hh = threadIdx.x >> 4;
+  const int64_t fb0 = static_cast<int64_t>(blockIdx.x) * U;
+  const int64_t tiles_m = (M + 15) / 16;
+  const int64_t up_off = FB * 16;  // the up half starts F channels (FB * 16 vectors) in
+  for (int64_t tm = blockIdx.y; tm < tiles_m; tm += gridDim.y) {
+    const int64_t row = tm * 16 + hh;
+    const bool row_ok = row < M;
+    const uint4* src = gu + row * ld_v + fb0 * 16 + lane16;
+    uint4 gv[U], uv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      gv[u] = uv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (row_ok && fb0 + u < FB) {
+        gv[u] = ld_nc_v4(src + u * 16);
+        uv[u] = ld_nc_v4(src + up_off + u * 16);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint4 h = make_uint4(swiglu_pair(gv[u].x, uv[u].x), swiglu_pair(gv[u].y, uv[u].y),
+                                 swiglu_pair(gv[u].z, uv[u].z), swiglu_pair(gv[u].w, uv[u].w));
+      uint32_t m = absmax8_pairs(h);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const GroupScale g = group_scale(pairs_to_max(m));
+      const int64_t fb = fb0 + u;
+      if (row_ok && fb < FB) {
+        q[row * ldq_v + fb * 16 + lane16] = quantise8(h, g);
+        if (lane16 == 0) sa[fb * ld_sa + row] = g.s;
+        if (h_out != nullptr) h_out[row * ldh_v + fb * 16 + lane16] = h;
+      }
+    }
+  }
+}
+
+constexpr int64_t kMaxGridY = 65535;
+
+}  // namespace
+
+cudaError_t launch_quant_per_token(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx, void* q,
+                                   int64_t ldq, float* s, cudaStream_t stream) {
+  const int64_t KV = K / 8;
+  const int64_t grid_cap = static_cast<int64_t>(dev.num_sms) * 8;
+  const int grid = static_cast<int>(M < grid_cap ? M : grid_cap);
+  const uint4* xv = static_cast<const uint4*>(x);
+  uint2* qv = static_cast<uint2*>(q);
+if (KV <= 256)
+    quant_per_token_kernel<1><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+  else if (KV <= 512)
+    quant_per_token_kernel<2><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+  else if (KV <= 1024)
+    quant_per_token_kernel<4><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+  else if (KV <= 2048)
+    quant_per_token_kernel<8><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+  else
+    quant_per_token_kernel<16><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_per_channel(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     void* q, int64_t ldq, float* s, cudaStream_t stream) {
+  (void)dev;
+  const int64_t KV = K / 8;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(s);
+  zero_words_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(bits, K);
+  const int64_t row_tiles = (M + 63) / 64;
+  const dim3 grid(static_cast<unsigned>((KV + 31) / 32),
+                  static_cast<unsigned>(row_tiles < kMaxGridY ? row_tiles : kMaxGridY));
+  channel_absmax_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), M, KV, ldx / 8, bits);
+  quant_per_channel_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), M, KV, ldx / 8, bits,
+                                                     static_cast<uint2*>(q), ldq / 8);
+  channel_scales_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(bits, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_e5m6(const DeviceInfo& dev, const void* x, int64_t n, void* codes, cudaStream_t stream) {
+  const int64_t nv = n / 8;
+  const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+  const int64_t blocks = (nv + 255) / 256;
+  cast_e5m6_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
+      static_cast<const uint4*>(x), nv, static_cast<uint4*>(codes));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e5m6_to_bf16(const DeviceInfo& dev, const void* codes, int64_t n, void* y, cudaStream_t stream) {
+  const int64_t nv = n / 8;
+  const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
+  const int64_t blocks = (nv + 255) / 256;
+  e5m6_to_bf16_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
+      static_cast<const uint4*>(codes), nv, static_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quant_act_1x128(const DeviceInfo& dev, const void* gate_up, int64_t M, int64_t F,
+                                          int64_t ld, void* q, int64_t ldq, float* sa, int64_t ld_sa, void* h,
+                                          int64_t ldh, cudaStream_t stream) {
+  (void)dev;
+  constexpr int kUnroll = 2;
+  const int64_t FB = F / 128;
+  const int64_t tiles_m = (M + 15) / 16;
+  const dim3 grid(static_cast<unsigned>((FB + kUnroll - 1) / kUnroll),
+                  static_cast<unsigned>(tiles_m < kMaxGridY ? tiles_m : kMaxGridY));
+  swiglu_quant_kernel<kUnroll><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(gate_up), M, FB, ld / 8,
+                                                         static_cast<uint2*>(q), ldq / 8, sa, ld_sa,
+                                                         static_cast<uint4*>(h), ldh / 8);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8bs

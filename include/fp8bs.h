@@ -203,6 +203,55 @@ fp8bs_status fp8_blockscaled_gemm_rowscaled_f32(const void* qa, int64_t ldqa, co
                                                 float* y_f32, int64_t ldy, int64_t M, int64_t N, int64_t K,
                                                 cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Quantisation variants.  The TileKernels release ("DeepSeek starts updating
+ * frequently", the tile kernels' features, item "Quantification") converts to
+ * FP8 / E5M6 per token, per block and per channel and fuses SwiGLU with the
+ * quantisation; the V3 excerpt (paragraph 3) keeps certain activations in a
+ * custom E5M6 format.  The FP8 variants use the 1x128 quantiser's rule
+ * s = fl32(amax / 448), codes E4M3_RNE_satfinite(fl32(x / s)).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Per token: one scale per row of X [M, K] BF16 over all K channels.
+ *   q : [M, K] codes (row stride ldq bytes);  s : [M] FP32 scales, contiguous.
+ * K % 8 == 0 and K <= 32768.
+ */
+fp8bs_status fp8_quant_per_token(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                                 float* s, cudaStream_t stream);
+
+/*
+ * Per channel: one scale per column of X [M, K] BF16 over all M rows.
+ *   q : [M, K] codes (row stride ldq);  s : [K] FP32 scales, contiguous,
+ *   16-byte aligned (used as the column-maximum accumulator while the call
+ *   runs).  K % 8 == 0.  X is read twice (maxima, then codes).
+ */
+fp8bs_status fp8_quant_per_channel(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
+                                   float* s, cudaStream_t stream);
+
+/*
+ * E5M6 activation format: sign, 5 exponent bits (bias 15), 6 mantissa bits
+ * in the low 12 bits of a 16-bit word; subnormals 2^-14 * m / 64; exponent
+ * field 31 reserved (decoded as inf / NaN).  Encoding rounds to nearest even
+ * and saturates magnitudes above 65024 (no scale factor).  n BF16 values in,
+ * n 16-bit codes out (n % 8 == 0, 16-byte aligned buffers); decoding back to
+ * BF16 is exact.
+ */
+fp8bs_status fp8bs_e5m6_encode_bf16(const void* x_bf16, int64_t n, void* codes_u16, cudaStream_t stream);
+fp8bs_status fp8bs_e5m6_decode_bf16(const void* codes_u16, int64_t n, void* y_bf16, cudaStream_t stream);
+
+/*
+ * SwiGLU fused with 1x128 quantisation.  gate_up : [M, 2F] BF16 (row stride
+ * ld): gate in columns [0, F), up projection in [F, 2F).
+ *   h = bf16_rn(silu(g) * u), silu(g) = g / (1 + exp(-g)) in FP32, and h is
+ *   quantised exactly as fp8_quant_act_1x128 would: qa [M, F] codes (stride
+ *   ldq), sa [F/128, ld_sa] scales.  h itself is written to h_bf16 (stride
+ *   ldh) when h_bf16 is not null.  F % 128 == 0.
+ */
+fp8bs_status fp8_swiglu_quant_act_1x128(const void* gate_up_bf16, int64_t M, int64_t F, int64_t ld,
+                                        void* qa, int64_t ldq, float* sa, int64_t ld_sa,
+                                        void* h_bf16, int64_t ldh, cudaStream_t stream);
+
 /*
  * Text naming the CUDA error (and the step) behind the last FP8BS_ERR_CUDA
  * returned to the calling host thread; "" if none.  Valid until the thread's

@@ -255,6 +255,96 @@ def blockscaled_grouped_gemm(offsets, qa, sa, qw, sw):
 
 
 # ---------------------------------------------------------------------------
+# Quantisation variants.  The TileKernels release ("DeepSeek starts updating
+# frequently", section on the tile kernels' features, item "Quantification")
+# converts to FP8/FP4/E5M6 "per token", "per block" and "per channel" and fuses
+# SwiGLU with the quantisation; the V3 excerpt keeps certain activations in a
+# custom E5M6 format (paragraph 3).  Readings: per token = one scale per row
+# of X [tokens, channels] over all its channels; per channel = one scale per
+# column over all tokens; both with the same amax / 448 rule as the 1x128
+# tiles.
+# ---------------------------------------------------------------------------
+
+def quant_per_token(x):
+    """One FP32 scale per row: codes [M, K], scales [M]."""
+    x = np.asarray(x, dtype=np.float32)
+    return _quantise_groups(x)
+
+
+def quant_per_channel(x):
+    """One FP32 scale per column: codes [M, K], scales [K]."""
+    x = np.asarray(x, dtype=np.float32)
+    codes, s = _quantise_groups(np.ascontiguousarray(x.T))
+    return np.ascontiguousarray(codes.T), s
+
+
+def silu_mul(gate, up):
+    """SwiGLU's product silu(g) * u = g / (1 + exp(-g)) * u in float64."""
+    g = np.asarray(gate, dtype=np.float64)
+    u = np.asarray(up, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def swiglu_quant_act_1x128(gate_up):
+    """SwiGLU then 1x128 quantisation.  gate_up float32 [M, 2F] holds the
+    gate in columns [0, F) and the up projection in [F, 2F) (BF16 values).
+    Reading: h = silu(g) * u is rounded to BF16 -- the activation the
+    quantiser sees is the one an unfused pipeline would store -- and then
+    quantised exactly as quant_act_1x128.  Returns (h float32 [M, F] holding
+    BF16 values, codes [M, F], scales [F/128, M])."""
+    gu = np.asarray(gate_up, dtype=np.float32)
+    F = gu.shape[1] // 2
+    h = bf16_round(silu_mul(gu[:, :F], gu[:, F:]).astype(np.float32))
+    qa, sa = quant_act_1x128(h)
+    return h, qa, sa
+
+
+# E5M6: sign, 5 exponent bits (bias 15), 6 mantissa bits in the low 12 bits of
+# a 16-bit word.  Reading (the pages give the name only): IEEE-style like
+# FP16 with the mantissa cut to 6 bits -- subnormals 2^-14 * m / 64, exponent
+# field 31 reserved (decoded as inf / NaN) -- encoded with round-to-nearest-
+# even and saturation to the largest finite value (1 + 63/64) * 2^15 = 65024,
+# without a scale factor.
+E5M6_MAX = 65024.0
+
+
+def e5m6_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint16).astype(np.int64) & 0xFFF
+    sign = c >> 11
+    exp = (c >> 6) & 0x1F
+    man = c & 0x3F
+    normal = np.ldexp(1.0 + man / 64.0, exp - 15)
+    subnormal = np.ldexp(man / 64.0, -14)
+    mag = np.where(exp == 0, subnormal, normal)
+    mag = np.where(exp == 31, np.where(man == 0, np.inf, np.nan), mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+_E5M6_POS_CODES = np.arange(31 << 6, dtype=np.int64)  # 0x000 .. 0x7BF, all finite non-negative
+_E5M6_POS_VALUES = e5m6_decode(_E5M6_POS_CODES.astype(np.uint16))
+
+
+def e5m6_encode_rne_satfinite(v) -> np.ndarray:
+    """E5M6 code of each float32 value: nearest representable value, ties to
+    the even code, magnitudes above 65024 saturate; the sign bit follows the
+    input's.  NaN inputs are outside the contract."""
+    v = np.asarray(v, dtype=np.float32)
+    a = np.abs(v).astype(np.float64)
+    hi = np.searchsorted(_E5M6_POS_VALUES, a, side="left")
+    saturate = hi >= len(_E5M6_POS_VALUES)
+    hi = np.minimum(hi, len(_E5M6_POS_VALUES) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E5M6_POS_VALUES[hi] - a
+    d_lo = a - _E5M6_POS_VALUES[lo]
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (_E5M6_POS_CODES[hi] % 2 == 0))
+    code = np.where(take_hi, hi, lo)
+    code = np.where(saturate, len(_E5M6_POS_VALUES) - 1, code)
+    code = code | (np.signbit(v).astype(np.int64) << 11)
+    return code.astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
 # Backward GEMMs of the FP8 linear layer.
 #
 # The excerpt trains with the same FP8 GEMMs: the activation is cached in FP8

@@ -618,6 +618,92 @@ def pin_backward_linearity(o):
         assert np.array_equal(dx1, dx0 * 2.0 ** j) and np.array_equal(dw1, dw0 * 2.0 ** j)
 
 
+# ---------------------------------------------------------------------------
+# Quantisation variants: per token, per channel, E5M6, SwiGLU + 1x128
+# ---------------------------------------------------------------------------
+
+def pin_e5m6_format(o):
+    """Every finite E5M6 code decodes to the FP16 value whose bit pattern is
+    the code shifted left by 4 (an E5M6 number is an FP16 number with the low
+    four mantissa bits zero: same sign, bias-15 exponent and subnormal
+    rule), checked against numpy's float16; 0x7C0 / 0x7C1 are inf / NaN."""
+    codes = np.array([c for c in range(4096) if ((c >> 6) & 0x1F) != 31], dtype=np.uint16)
+    want = (codes.astype(np.uint16) << 4).view(np.float16).astype(np.float64)
+    got = o.e5m6_decode(codes)
+    assert np.array_equal(got, want)
+    special = o.e5m6_decode(np.array([0x7C0, 0x7C1, 0xFC0], dtype=np.uint16))
+    assert np.isinf(special[0]) and np.isnan(special[1]) and special[2] == -np.inf
+    assert o.E5M6_MAX == 65024.0 and float(o.e5m6_decode(np.array([0x7BF], dtype=np.uint16))[0]) == 65024.0
+
+
+def pin_e5m6_roundtrip_and_ties(o):
+    codes = np.array([c for c in range(4096) if ((c >> 6) & 0x1F) != 31], dtype=np.uint16)
+    vals = o.e5m6_decode(codes)
+    assert np.array_equal(o.e5m6_encode_rne_satfinite(vals.astype(np.float32)), codes)
+    pos = o.e5m6_decode(np.arange(31 << 6, dtype=np.uint16))
+    assert np.all(np.diff(pos) > 0)
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (pos[:-1] + pos[1:]) / 2)  # exact in float32
+    even = np.where(np.arange(len(mids)) % 2 == 0, np.arange(len(mids)), np.arange(len(mids)) + 1)
+    for sgn, sbit in ((1, 0), (-1, 0x800)):
+        got = o.e5m6_encode_rne_satfinite(sgn * mids)
+        assert np.array_equal(got.astype(np.int64), even | sbit)
+        up = np.nextafter(sgn * mids, np.float32(sgn * np.inf), dtype=np.float32)
+        assert np.array_equal(o.e5m6_encode_rne_satfinite(up).astype(np.int64), (np.arange(len(mids)) + 1) | sbit)
+    big = np.array([65024.0, 65279.0, 65280.0, 70000.0, 3e38], dtype=np.float32)
+    assert np.all(o.e5m6_encode_rne_satfinite(big) == 0x7BF) and np.all(o.e5m6_encode_rne_satfinite(-big) == 0xFBF)
+    assert list(o.e5m6_encode_rne_satfinite(np.array([0.0, -0.0, -1e-30], dtype=np.float32))) == [0, 0x800, 0x800]
+
+
+def pin_per_token_and_channel(o):
+    """Per-token groups are whole rows, per-channel groups whole columns:
+    constant rows / columns code to +-448 with s = fl32(|c| / 448); per
+    channel equals per token of the transpose; one element changes only its
+    own row's (column's) scale and codes."""
+    rng = np.random.default_rng(67)
+    c = (rng.standard_normal(5) * 3).astype(np.float32)
+    q, s = o.quant_per_token(np.tile(c[:, None], (1, 300)))
+    assert q.shape == (5, 300) and s.shape == (5,)
+    assert np.all((q == 0x7E) | (q == 0xFE))
+    for i in range(5):
+        assert s[i] == _nearest_f32(Fraction(float(abs(c[i]))) / 448)
+    x = rng.standard_normal((40, 300)).astype(np.float32)
+    qc, sc = o.quant_per_channel(x)
+    qt, st = o.quant_per_token(np.ascontiguousarray(x.T))
+    assert np.array_equal(qc, qt.T) and np.array_equal(sc, st) and sc.shape == (300,)
+    amax_col = np.argmax(np.abs(x), axis=0)
+    assert np.all(np.isin(qc[amax_col, np.arange(300)], (0x7E, 0xFE)))
+    x2 = x.copy()
+    x2[7, 11] = 1000.0
+    q0, s0 = o.quant_per_token(x)
+    q1, s1 = o.quant_per_token(x2)
+    assert set(np.nonzero(q0 != q1)[0]) == {7} and set(np.nonzero(s0 != s1)[0]) == {7}
+    q0, s0 = o.quant_per_channel(x)
+    q1, s1 = o.quant_per_channel(x2)
+    assert set(np.nonzero(q0 != q1)[1]) == {11} and set(np.nonzero(s0 != s1)[0]) == {11}
+
+
+def pin_swiglu(o):
+    """silu(g) - silu(-g) = g (sigmoid(g) + sigmoid(-g) = 1), silu(ln 3) =
+    0.75 ln 3, silu(0) = 0; h rounds silu(gate) * up to BF16 with the gate in
+    the first half of each row and the up projection in the second; the
+    codes are the 1x128 quantisation of h."""
+    g = np.linspace(-20, 20, 4001)
+    d = o.silu_mul(g, np.ones_like(g)) - o.silu_mul(-g, np.ones_like(g))
+    assert np.all(np.abs(d - g) <= 1e-14 * np.maximum(1, np.abs(g)))
+    assert abs(o.silu_mul(np.log(3.0), 1.0) - 0.75 * np.log(3.0)) < 1e-15 and o.silu_mul(0.0, 5.0) == 0.0
+    rng = np.random.default_rng(71)
+    gate = (rng.standard_normal((3, 256)) * 2).astype(np.float32)
+    up = rng.standard_normal((3, 256)).astype(np.float32)
+    h, qa, sa = o.swiglu_quant_act_1x128(np.concatenate([gate, up], axis=1))
+    want = gate.astype(np.float64) / (1 + np.exp(-gate.astype(np.float64))) * up
+    assert np.array_equal(h, o.bf16_round(want.astype(np.float32)))
+    q2, s2 = o.quant_act_1x128(h)
+    assert np.array_equal(qa, q2) and np.array_equal(sa, s2)
+    h0, _, _ = o.swiglu_quant_act_1x128(np.concatenate([np.zeros_like(gate), up], axis=1))
+    assert np.all(h0 == 0)
+
+
 ALL_PINS = [
     pin_codec_format_points,
     pin_codec_roundtrip,
@@ -647,4 +733,8 @@ ALL_PINS = [
     pin_transposed_quant_structure,
     pin_backward_error_bound,
     pin_backward_linearity,
+    pin_e5m6_format,
+    pin_e5m6_roundtrip_and_ties,
+    pin_per_token_and_channel,
+    pin_swiglu,
 ]

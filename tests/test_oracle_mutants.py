@@ -93,6 +93,21 @@ MUTANTS = {
     "transposed_quant_not_transposed": (
         "return quant_act_1x128(np.ascontiguousarray(x.T))",
         "return quant_act_1x128(x)"),
+    "e5m6_bias_16": (
+        "normal = np.ldexp(1.0 + man / 64.0, exp - 15)",
+        "normal = np.ldexp(1.0 + man / 64.0, exp - 16)"),
+    "e5m6_ties_away": (
+        "take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (_E5M6_POS_CODES[hi] % 2 == 0))",
+        "take_hi = (d_hi <= d_lo)"),
+    "per_channel_is_per_token": (
+        "codes, s = _quantise_groups(np.ascontiguousarray(x.T))\n    return np.ascontiguousarray(codes.T), s",
+        "codes, s = _quantise_groups(x)\n    return codes, s"),
+    "swiglu_gate_up_swapped": (
+        "h = bf16_round(silu_mul(gu[:, :F], gu[:, F:]).astype(np.float32))",
+        "h = bf16_round(silu_mul(gu[:, F:], gu[:, :F]).astype(np.float32))"),
+    "silu_sign_flipped": (
+        "return g / (1.0 + np.exp(-g)) * u",
+        "return g / (1.0 + np.exp(g)) * u"),
     "grouped_wrong_weight_scales": (
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])",
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[0])"),
