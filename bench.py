@@ -542,16 +542,23 @@ def run_reference(args):
 # size, against its roofline, with the CPU oracle timed on a bounded sample
 # in the same unit.  One JSON line per row (not the default line).
 # ---------------------------------------------------------------------------
-def _time_kernel(fn, iters=20, warmup=3):
-    """Median CUDA-event time (ms) of fn() on the current stream, with a
-    512 MB write between iterations so no input is L2-resident."""
-    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+_FLUSH = None
+
+
+def _time_kernel(fn, iters=40, warmup=3):
+    """Median CUDA-event time (ms) of fn() on the current stream.  Between
+    iterations a 512 MB buffer is read (a sum), which evicts every input from
+    L2 without leaving dirty lines whose write-back would be charged to the
+    timed kernel."""
+    global _FLUSH
+    if _FLUSH is None:
+        _FLUSH = torch.ones(128 * 2 ** 20, dtype=torch.float32, device="cuda")
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     ts = []
     for _ in range(iters):
-        flush.zero_()
+        _FLUSH.sum()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -559,8 +566,11 @@ def _time_kernel(fn, iters=20, warmup=3):
         b.record()
         b.synchronize()
         ts.append(a.elapsed_time(b))
+    # event timestamps are coarse (a few microseconds apart for short kernels):
+    # average the middle half instead of taking a median
     ts.sort()
-    return ts[len(ts) // 2]
+    mid = ts[len(ts) // 4: len(ts) - len(ts) // 4]
+    return sum(mid) / len(mid)
 
 
 def _time_cpu(fn, budget_s=2.0):

@@ -83,6 +83,7 @@ struct Params {
   int64_t ldy;
   int32_t M;            // rows of A (M_total when grouped)
   int32_t N;
+  int32_t n_fastest;    // dense: walk tiles N-fastest (A is the larger operand)
   int32_t KB;           // K / 128
   const int32_t* offsets;  // grouped only, [G+1]
   int32_t G;
@@ -90,13 +91,20 @@ struct Params {
   uint64_t timeout_ns;
 };
 
-template <int BN, int STAGES, int CG, bool RS = false>
+// Shared-memory layout.  Stage s holds its A tile at a_off(s) and its share
+// of the B tile at b_off(s).  HALF_A (M <= 64): only 64 rows of A are loaded
+// and each stage is laid out [A 8 KB][B], so the M = 128 MMA's read of A rows
+// 64 .. 127 falls on the same stage's B bytes, which have landed; those
+// accumulator rows are never stored.
+template <int BN, int STAGES, int CG, bool RS = false, bool HALF_A = false>
 struct Smem {
-  static constexpr int kA = BM * BK;
+  static constexpr int kARows = HALF_A ? BM / 2 : BM;
+  static constexpr int kA = kARows * BK;
   static constexpr int kB = (BN / CG) * BK;  // this CTA's share of the B tile
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + STAGES * kA;
-  static constexpr int kOffStaging = kOffB + STAGES * kB;
+  static constexpr int kStage = kA + kB;
+  __host__ __device__ static constexpr uint32_t a_off(uint32_t s) { return HALF_A ? s * kStage : s * kA; }
+  __host__ __device__ static constexpr uint32_t b_off(uint32_t s) { return HALF_A ? s * kStage + kA : STAGES * kA + s * kB; }
+  static constexpr int kOffStaging = STAGES * kStage;
   // row-scaled B: per promotion warp, two chunks x (BN / 2) column scales
   static constexpr int kOffColScale = kOffStaging + kEpiWarps * kStagingBytes;
   static constexpr int kColScaleBytes = RS ? kEpiWarps * 2 * (BN / 2) * 4 : 0;
@@ -108,7 +116,8 @@ struct Smem {
   static constexpr int kDynamic = kBytes + 1024;  // + alignment slack
 };
 
-// Tile walker shared by all roles.  Tiles are visited in "cluster tiles" of
+// Tile walker shared by all roles (dense tiles in M-fastest or N-fastest order,
+// see Params::n_fastest).  Tiles are visited in "cluster tiles" of
 // CM consecutive 128-row tiles x one BN-column tile; the CM CTAs of a
 // cluster walk the same cluster tiles in the same order and CTA `rank` takes
 // row tile CM * m + rank of each.  Yields (a_row, row_end, b_row, n0, group)
@@ -151,8 +160,11 @@ struct TileWalker {
     if (!GROUPED) {
       const int32_t m_groups = ((p.M + BM - 1) / BM + CM - 1) / CM;
       if (t >= static_cast<int64_t>(m_groups) * n_tiles) return false;
-      const int32_t mg = static_cast<int32_t>(t % m_groups);
-      const int32_t nt = static_cast<int32_t>(t / m_groups);
+      // M-fastest keeps a wave on a few weight column tiles and streams A,
+      // which stays L2-resident when it is the smaller operand; otherwise
+      // walk N-fastest so the smaller B is the one re-read from L2
+      const int32_t mg = static_cast<int32_t>(p.n_fastest ? t / n_tiles : t % m_groups);
+      const int32_t nt = static_cast<int32_t>(p.n_fastest ? t % n_tiles : t / m_groups);
       a_row = (mg * CM + rank) * BM;
       row_end = p.M;
       n0 = nt * BN;
@@ -184,11 +196,12 @@ __device__ __forceinline__ void abort_cta(volatile int* abort_flag, unsigned* st
   record_status(status, kStatusTimeout);
 }
 
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false>
 __global__ void __launch_bounds__(kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmY, const Params p) {
-  using L = Smem<BN, STAGES, CG, RS>;
+  using L = Smem<BN, STAGES, CG, RS, HALF_A>;
+  static_assert(!HALF_A || (CG == 1 && !GROUPED), "64-row A tiles are a dense single-CTA variant");
   static_assert(!(RS && GROUPED), "row-scaled B is a dense-only variant");
   static_assert(CG == 1 || CG == 2, "single CTAs or CTA pairs");
   constexpr int kTmemCols = 2 * BN;   // two accumulator buffers of this CTA's 128 rows x BN
@@ -274,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t a_dst = base + L::kOffA + stage * L::kA;
-          const uint32_t b_dst = base + L::kOffB + stage * L::kB;
+          const uint32_t a_dst = base + L::a_off(stage);
+          const uint32_t b_dst = base + L::b_off(stage);
           if (CG == 1) {
             const uint32_t full = bar_full + 8 * stage;
             mbar_arrive_expect_tx(full, kStageTx);
@@ -329,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t d = tmem_base + buf * BN;
-          const uint64_t adesc = smem_desc_k128_sw128(base + L::kOffA + stage * L::kA);
-          const uint64_t bdesc = smem_desc_k128_sw128(base + L::kOffB + stage * L::kB);
+          const uint64_t adesc = smem_desc_k128_sw128(base + L::a_off(stage));
+          const uint64_t bdesc = smem_desc_k128_sw128(base + L::b_off(stage));
 #pragma unroll
           for (int k = 0; k < BK / MMA_K; ++k) {
             // advance the start address by 32 bytes (2 units of 16 B) per K step
@@ -373,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* staging_ptr = smem + L::kOffStaging + epi * kStagingBytes;
     uint32_t buf = 0, bphase = 0;
     bool ok = true;
+    const bool live = !HALF_A || q < 2;  // the warp's TMEM lanes can hold output rows
     while (ok && tiles.get(a_row, row_end, b_row, n0, group)) {
       const int32_t row = a_row + q * 32 + lane;  // this thread's output row
       const bool row_ok = row < row_end;
@@ -419,8 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + half * kHalfCols;
+        if (!live) {
+          // lanes 64 .. 127 of a 64-row A tile hold no output: release at once
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_relaxed(bar_tempty + 8 * buf);
+        }
 #pragma unroll
-        for (int c = 0; c < kHalfCols / 64; ++c) {
+        for (int c = 0; c < (live ? kHalfCols / 64 : 0); ++c) {
           uint32_t r[64];
           tmem_ld_x64(taddr + c * 64, r);
           tmem_wait_ld(r);
@@ -475,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- epilogue: BF16 (RNE) or FP32, swizzled staging, store ----
 #pragma unroll
-      for (int piece = 0; piece < kHalfCols / kPieceCols; ++piece) {
+      for (int piece = 0; piece < (live ? kHalfCols / kPieceCols : 0); ++piece) {
         if (!GROUPED) {
           if (lane == 0) tma_store_wait_read_all();  // staging free again
         }
@@ -548,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Largest number of clusters of this kernel variant that can be resident at
 // once on the current device (queried once per device and variant).
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A>
 int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) {
   static std::atomic<int> cache[64];
   const int idx = dev.ordinal & 63;
@@ -557,7 +577,7 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
   n = dev.num_sms / CG;
   if (CG > 1) {
     int q = 0;
-    if (cudaOccupancyMaxActiveClusters(&q, blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS>, &cfg) == cudaSuccess &&
+    if (cudaOccupancyMaxActiveClusters(&q, blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>, &cfg) == cudaSuccess &&
         q > 0)
       n = q;
     else
@@ -569,11 +589,11 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
 
 // Persistent launch: one cluster of CG CTAs per CG SMs, at most one per
 // cluster tile.
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false>
 cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                           const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream) {
-  using L = Smem<BN, STAGES, CG, RS>;
-  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS>;
+  using L = Smem<BN, STAGES, CG, RS, HALF_A>;
+  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>;
   if (BN == 256) {
     // setmaxnreg.inc only completes if the launch holds kRegsLaunch registers
     // per thread; refuse to launch a build that does not.
@@ -596,7 +616,7 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(CG, 1, 1);
-  const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32, RS>(dev, cfg);
+  const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>(dev, cfg);
   const int64_t clusters = cluster_tiles < resident ? cluster_tiles : resident;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmY, p);
@@ -609,6 +629,7 @@ constexpr int kStagesPair = 6;   // BN = 256 on a CTA pair: 32 KB stages
 constexpr bool kUsePairs = true;
 constexpr int kStages256 = 4;    // BN = 256 on one CTA: 48 KB stages
 constexpr int kStages128 = 6;    // BN = 128 on one CTA: 32 KB stages
+constexpr int kStages128HalfA = 8;  // BN = 128, 64-row A tiles (M <= 64): 24 KB stages
 // Row-scaled B stages its column scales in shared memory: one stage fewer.
 constexpr int kStagesPairRS = 5;
 constexpr int kStages256RS = 3;
@@ -619,6 +640,7 @@ static_assert(Smem<128, kStages128RS, 1, true>::kDynamic <= 232448, "shared memo
 static_assert(Smem<256, kStagesPair, 2>::kDynamic <= 232448, "shared memory budget (BN=256, pair)");
 static_assert(Smem<256, kStages256, 1>::kDynamic <= 232448, "shared memory budget (BN=256)");
 static_assert(Smem<128, kStages128, 1>::kDynamic <= 232448, "shared memory budget (BN=128)");
+static_assert(Smem<128, kStages128HalfA, 1, false, true>::kDynamic <= 232448, "shared memory budget (64-row A)");
 
 Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const float* sw, void* y, int64_t ldy,
                    int64_t M, int64_t N, int64_t K, const int32_t* offsets, int32_t G) {
@@ -632,6 +654,7 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
   p.ldy = ldy;
   p.M = static_cast<int32_t>(M);
   p.N = static_cast<int32_t>(N);
+  p.n_fastest = M > N ? 1 : 0;
   p.KB = static_cast<int32_t>(K / BK);
   p.offsets = offsets;
   p.G = G;
@@ -643,7 +666,7 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
 
 // Tile shapes: narrow (BN = 128, one CTA), wide (BN = 256, one CTA) and
 // pair (BN = 256 on a CTA pair, 256 x 256 per pair).
-enum class Shape { kNarrow, kWide, kPair };
+enum class Shape { kNarrow, kNarrowHalfA, kWide, kPair };
 
 template <bool GROUPED, bool F32, bool RS = false>
 cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -652,6 +675,11 @@ cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& 
     case Shape::kNarrow:
       return launch_kernel<128, RS ? kStages128RS : kStages128, GROUPED, 1, F32, RS>(dev, tmA, tmB, tmY, p,
                                                                                       cluster_tiles, stream);
+    case Shape::kNarrowHalfA:
+      if constexpr (!GROUPED && !RS)
+        return launch_kernel<128, kStages128HalfA, false, 1, F32, false, true>(dev, tmA, tmB, tmY, p, cluster_tiles,
+                                                                             stream);
+      return cudaErrorInvalidValue;
     case Shape::kWide:
       return launch_kernel<256, RS ? kStages256RS : kStages256, GROUPED, 1, F32, RS>(dev, tmA, tmB, tmY, p,
                                                                                       cluster_tiles, stream);
@@ -671,12 +699,14 @@ cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64
   // every SM busy when there are few tiles (skinny, decode-shaped M).
   const int64_t m_tiles = (M + BM - 1) / BM;
   const bool wide = (N % 256 == 0) && m_tiles * (N / 256) >= dev.num_sms;
-  const Shape shape = !wide ? Shape::kNarrow : (kUsePairs && m_tiles >= 2 ? Shape::kPair : Shape::kWide);
+  const Shape shape = !wide ? (M <= BM / 2 ? Shape::kNarrowHalfA : Shape::kNarrow)
+                             : (kUsePairs && m_tiles >= 2 ? Shape::kPair : Shape::kWide);
   const int CG = shape == Shape::kPair ? 2 : 1;
   const int BN = wide ? 256 : 128;
   const int out_bytes = y_f32 ? 4 : 2;
+  const uint32_t a_rows = shape == Shape::kNarrowHalfA ? BM / 2 : BM;
   CUtensorMap tmA, tmB, tmY;
-  if (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, BK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, N, ldqw, BK, BN / CG, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d(&tmY, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M,
                     ldy * out_bytes, kEpiRowBytes / out_bytes, 32, CU_TENSOR_MAP_SWIZZLE_128B))

@@ -188,6 +188,48 @@ __device__ __forceinline__ uint2 quantise8(const uint4 v, const GroupScale& g) {
   return make_uint2(lo0, lo1);
 }
 
+// Quantise 8 BF16 values that belong to 8 different groups (one scale per
+// column, e.g. per-channel groups): g points at the 8 groups' constants and
+// special0 / special1 mark (0xFF per byte) the elements whose scale is zero
+// or subnormal.  Straddling and special elements are fixed one by one.
+__device__ __forceinline__ uint32_t fix_word_cols(uint32_t lo, uint32_t diff, uint32_t w0, uint32_t w1, float s0,
+                                                  float s1, float s2, float s3) {
+  while (diff != 0u) {
+    const int byte = (__ffs(diff) - 1) >> 3;
+    const uint32_t word = byte < 2 ? w0 : w1;
+    const float x = (byte & 1) ? bf16hi_to_f32(word) : bf16lo_to_f32(word);
+    const float sc = byte == 0 ? s0 : byte == 1 ? s1 : byte == 2 ? s2 : s3;
+    const uint32_t code = sc == 0.0f ? 0u : (cvt_e4m3x4(__fdiv_rn(x, sc), 0.0f, 0.0f, 0.0f) & 0xFFu);
+    lo = (lo & ~(0xFFu << (8 * byte))) | (code << (8 * byte));
+    diff &= ~(0xFFu << (8 * byte));
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint2 quantise8_cols(const uint4 v, const GroupScale (&g)[8], uint32_t special0,
+                                                uint32_t special1) {
+  const float2 a = bf16x2_to_f32x2(v.x), b = bf16x2_to_f32x2(v.y);
+  const float2 c = bf16x2_to_f32x2(v.z), d = bf16x2_to_f32x2(v.w);
+  const float2 al = __fmul2_rn(a, make_float2(g[0].r_lo.x, g[1].r_lo.x));
+  const float2 ah = __fmul2_rn(a, make_float2(g[0].r_hi.x, g[1].r_hi.x));
+  const float2 bl = __fmul2_rn(b, make_float2(g[2].r_lo.x, g[3].r_lo.x));
+  const float2 bh = __fmul2_rn(b, make_float2(g[2].r_hi.x, g[3].r_hi.x));
+  const float2 cl = __fmul2_rn(c, make_float2(g[4].r_lo.x, g[5].r_lo.x));
+  const float2 ch = __fmul2_rn(c, make_float2(g[4].r_hi.x, g[5].r_hi.x));
+  const float2 dl = __fmul2_rn(d, make_float2(g[6].r_lo.x, g[7].r_lo.x));
+  const float2 dh = __fmul2_rn(d, make_float2(g[6].r_hi.x, g[7].r_hi.x));
+  uint32_t lo0 = cvt_e4m3x4(al.x, al.y, bl.x, bl.y);
+  const uint32_t hi0 = cvt_e4m3x4(ah.x, ah.y, bh.x, bh.y);
+  uint32_t lo1 = cvt_e4m3x4(cl.x, cl.y, dl.x, dl.y);
+  const uint32_t hi1 = cvt_e4m3x4(ch.x, ch.y, dh.x, dh.y);
+  const uint32_t diff0 = (lo0 ^ hi0) | special0, diff1 = (lo1 ^ hi1) | special1;
+  if ((diff0 | diff1) != 0u) {
+    lo0 = fix_word_cols(lo0, diff0, v.x, v.y, g[0].s, g[1].s, g[2].s, g[3].s);
+    lo1 = fix_word_cols(lo1, diff1, v.z, v.w, g[4].s, g[5].s, g[6].s, g[7].s);
+  }
+  return make_uint2(lo0, lo1);
+}
+
 // Code of a single value with its own group's scale (the per-element form of
 // quantise8, for groups that run across vectors).
 __device__ __forceinline__ uint32_t quantise1(float x, const GroupScale& g) {

@@ -110,24 +110,22 @@ __global__ void __launch_bounds__(256) quant_per_channel_kernel(const uint4* __r
   const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   if (col_v >= KV) return;
   GroupScale g[8];  // the scales of this thread's 8 columns
+  uint32_t special0 = 0u, special1 = 0u;  // zero or subnormal scales, 0xFF per element
 #pragma unroll
-  for (int c = 0; c < 8; ++c) g[c] = group_scale(__uint_as_float(__ldg(amax_bits + col_v * 8 + c) << 16));
+  for (int c = 0; c < 8; ++c) {
+    g[c] = group_scale(__uint_as_float(__ldg(amax_bits + col_v * 8 + c) << 16));
+    const uint32_t mark = (g[c].s == 0.0f || !g[c].bracket_ok) ? 0xFFu : 0u;
+    if (c < 4)
+      special0 |= mark << (8 * c);
+    else
+      special1 |= mark << (8 * (c - 4));
+  }
   const int64_t row_tiles = (M + 63) / 64;
   for (int64_t tile = blockIdx.y; tile < row_tiles; tile += gridDim.y) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int64_t row = tile * 64 + r8 + 8 * i;
-      if (row < M) {
-        const uint4 v = ld_nc_v4(x + row * ldx_v + col_v);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[2] = {0u, 0u};
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float xv = (c & 1) ? bf16hi_to_f32(w[c >> 1]) : bf16lo_to_f32(w[c >> 1]);
-          out[c >> 2] |= quantise1(xv, g[c]) << (8 * (c & 3));
-        }
-        q[row * ldq_v + col_v] = make_uint2(out[0], out[1]);
-      }
+      if (row < M) q[row * ldq_v + col_v] = quantise8_cols(ld_nc_v4(x + row * ldx_v + col_v), g, special0, special1);
     }
   }
 }
