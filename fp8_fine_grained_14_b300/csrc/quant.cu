@@ -27,39 +27,44 @@ namespace {
 // ---------------------------------------------------------------------------
 // 1x128 activation tiles.
 //
-// Grid: x over groups of U consecutive 128-channel groups, y over tiles of 16
-// rows.  A CTA of 256 threads = 16 half-warps; half-warp h owns row
-// (16 * tile + h) and its 16 lanes hold 8 channels each of a group.  The U
-// loads of a thread are issued before any arithmetic.
+// Grid: x over groups of U consecutive 128-channel groups, y over tiles of 32
+// rows.  A CTA of 256 threads = 32 eight-lane teams; team r owns row
+// (32 * tile + r) and each of its 8 lanes holds 16 channels (two 16-byte
+// vectors) of a group, so the codes leave as one 16-byte store per lane.  The
+// 2U loads of a thread are issued before any arithmetic.
 // ---------------------------------------------------------------------------
 template <int U>
 __global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint4* __restrict__ x, int64_t M, int64_t KB,
-                                                              int64_t ldx_v, uint2* __restrict__ q, int64_t ldq_v,
+                                                              int64_t ldx_v, uint4* __restrict__ q, int64_t ldq_v,
                                                               float* __restrict__ sa, int64_t ld_sa) {
-  const int lane16 = threadIdx.x & 15;
-  const int h = threadIdx.x >> 4;
+  const int lane8 = threadIdx.x & 7;
+  const int r = threadIdx.x >> 3;  // 32 rows per CTA
   const int64_t kb0 = static_cast<int64_t>(blockIdx.x) * U;
-  const int64_t tiles_m = (M + 15) / 16;
+  const int64_t tiles_m = (M + 31) / 32;
   for (int64_t tm = blockIdx.y; tm < tiles_m; tm += gridDim.y) {
-    const int64_t row = tm * 16 + h;
+    const int64_t row = tm * 32 + r;
     const bool row_ok = row < M;
-    const uint4* src = x + row * ldx_v + kb0 * 16 + lane16;
-    uint4 v[U];
+    const uint4* src = x + row * ldx_v + kb0 * 16 + lane8 * 2;
+    uint4 v[U][2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (row_ok && kb0 + u < KB) v[u] = ld_nc_v4(src + u * 16);
+      v[u][0] = v[u][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (row_ok && kb0 + u < KB) {
+        v[u][0] = ld_nc_v4(src + u * 16);
+        v[u][1] = ld_nc_v4(src + u * 16 + 1);
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      uint32_t m = absmax8_pairs(v[u]);
+      uint32_t m = max_pairs(absmax8_pairs(v[u][0]), absmax8_pairs(v[u][1]));
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
+      for (int off = 4; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
       const GroupScale g = group_scale(pairs_to_max(m));
       const int64_t kb = kb0 + u;
       if (row_ok && kb < KB) {
-        q[row * ldq_v + kb * 16 + lane16] = quantise8(v[u], g);
-        if (lane16 == 0) sa[kb * ld_sa + row] = g.s;
+        const uint2 c0 = quantise8(v[u][0], g), c1 = quantise8(v[u][1], g);
+        q[row * ldq_v + kb * 8 + lane8] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+        if (lane8 == 0) sa[kb * ld_sa + row] = g.s;
       }
     }
   }
@@ -173,11 +178,11 @@ cudaError_t launch_quant_act_1x128(const DeviceInfo& dev, const void* x, int64_t
   // CTAs short (the grid is several waves of 8 resident CTAs per SM).
   constexpr int kUnroll = 2;
   const int64_t KB = K / 128;
-  const int64_t tiles_m = (M + 15) / 16;
+  const int64_t tiles_m = (M + 31) / 32;
   const dim3 grid(static_cast<unsigned>((KB + kUnroll - 1) / kUnroll),
                   static_cast<unsigned>(tiles_m < kMaxGridY ? tiles_m : kMaxGridY));
   quant_act_1x128_kernel<kUnroll><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), M, KB, ldx / 8,
-                                                            static_cast<uint2*>(q), ldq / 8, sa, ld_sa);
+                                                            static_cast<uint4*>(q), ldq / 16, sa, ld_sa);
   return cudaGetLastError();
 }
 
