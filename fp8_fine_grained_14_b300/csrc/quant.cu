@@ -9,9 +9,9 @@
 //
 // Both kernels are HBM-bound (2 bytes read, 1 byte + 4/group written per
 // element), so the arithmetic per element is kept to a handful of
-// instructions: packed BF16 abs-max, a division-free exact scale, packed FP32
-// products against a bracketing reciprocal, and the hardware E4M3 pair
-// conversion.  The build never enables fast math or flush-to-zero; codes and
+// instructions: packed BF16 abs-max, a division-free exact scale, the exact
+// quotient from a correctly rounded reciprocal and one packed FMA correction,
+// and the hardware E4M3 pair conversion.  The build never enables fast math or flush-to-zero; codes and
 // scales are bit-identical to the float32 definition (see group_scale and
 // quantise8 for why).
 #include <cuda_bf16.h>

@@ -110,11 +110,11 @@ __global__ void __launch_bounds__(256) quant_per_channel_kernel(const uint4* __r
   const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   if (col_v >= KV) return;
   GroupScale g[8];  // the scales of this thread's 8 columns
-  uint32_t special0 = 0u, special1 = 0u;  // zero or subnormal scales, 0xFF per element
+  uint32_t special0 = 0u, special1 = 0u;  // zero scales or scales below 2^-64, 0xFF per element
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     g[c] = group_scale(__uint_as_float(__ldg(amax_bits + col_v * 8 + c) << 16));
-    const uint32_t mark = (g[c].s == 0.0f || !g[c].bracket_ok) ? 0xFFu : 0u;
+    const uint32_t mark = (g[c].s == 0.0f || !g[c].fast) ? 0xFFu : 0u;
     if (c < 4)
       special0 |= mark << (8 * c);
     else

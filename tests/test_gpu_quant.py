@@ -72,14 +72,20 @@ def test_act_quant_exact_ties_and_edges():
     z = np.zeros((1, 128), dtype=np.float32)
     z[0, 5] = -0.0
     rows.append(z)
-    for e in (-133, -126, -120, -60, 60, 120):
+    # -126 .. -60: scales far below 2^-64 (IEEE division path); -58 .. -52:
+    # amax around 448 * 2^-64, where the exact FMA-corrected quotient takes over
+    for e in (-133, -126, -120, -60, -58, -57, -56, -55, -54, -52, 60, 120):
         rows.append((rng.standard_normal((1, 128)) * 2.0 ** e).astype(np.float32))
+    negz = rng.standard_normal((1, 128)).astype(np.float32)
+    negz[0, 3:9] = -0.0  # -0 inside a non-zero group codes as 0x80
+    rows.append(negz)
     mixed = rng.standard_normal((1, 128)).astype(np.float32)
     mixed[0, :10] = -(2.0 ** -20)  # far below the group's E4M3 resolution: -0 codes
     rows.append(mixed)
     x = torch.from_numpy(np.concatenate(rows)).to(torch.bfloat16)
     qa, _ = _act_parity(x)
     assert u8(qa)[len(x_ties), 5] == 0x00  # -0 in an all-zero group codes as +0
+    assert np.all(u8(qa)[-2, 3:9] == 0x80)
     assert np.all(u8(qa)[-1, :10] == 0x80)
 
 
@@ -181,11 +187,33 @@ def test_act_quant_every_bf16_magnitude():
     _act_parity(torch.from_numpy(x).to(torch.bfloat16))
 
 
+def test_act_quant_all_significand_pairs():
+    """Every (amax significand, x significand) pair at every exponent offset
+    that gives a non-zero code or the zero boundary, both signs.  amax and x
+    are BF16, so s = fl32(amax / 448) has 128 possible significands and this
+    covers the quotient x / s exhaustively up to powers of two."""
+    sig = 1.0 + np.arange(128) / 128.0
+    groups = []
+    for a in sig:
+        for d in range(-20, 1):
+            xs = sig * 2.0 ** d * 4.0
+            if d == 0:
+                xs = np.where(sig <= a, xs, a * 4.0)  # stay below the group's amax
+            for sign in (1.0, -1.0):
+                g = np.concatenate([[a * 4.0], sign * xs[:127]])
+                groups.append(g)
+                groups.append(np.concatenate([[a * 4.0], sign * xs[127:], np.zeros(126)]))
+    x = np.asarray(groups, dtype=np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(f32(xb), x), "inputs must be BF16-exact"
+    _act_parity(xb)
+
+
 @pytest.mark.parametrize("M,K", [(4096, 4096)])
 def test_act_quant_random_sweep(M, K):
     """16.7M elements with a random power-of-two magnitude per row: every code
-    and scale matches the oracle (exercises both the bracketing fast path
-    and its division fallback on near-boundary quotients)."""
+    and scale matches the oracle (the FMA-corrected quotient and, for rows
+    with scales below 2^-64, the IEEE division)."""
     g = torch.Generator().manual_seed(123)
     x = torch.randn(M, K, generator=g) * torch.pow(2.0, torch.randint(-40, 40, (M, 1), generator=g).float())
     _act_parity(x.to(torch.bfloat16))
