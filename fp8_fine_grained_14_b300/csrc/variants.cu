@@ -206,56 +206,81 @@ __global__ void __launch_bounds__(256) e5m6_to_bf16_kernel(const uint4* __restri
 }
 
 // ---------------------------------------------------------------------------
-// SwiGLU + 1x128 quantisation: h = bf16(silu(g) * u), silu(g) = g / (1 +
-// exp(-g)) in float32 (expf and the IEEE division), then the 1x128 quantiser
-// on the BF16 h.  Layout and tiling as the activation quantiser: grid x over
-// pairs of 128-channel groups of h, y over 16-row tiles; half-warp per row.
+// SwiGLU + 1x128 quantisation: h = bf16(silu(g) * u) with silu(g) = g / (1 +
+// exp(-g)) = g * sigmoid(g), evaluated in float32 from t = expf(-|g|), which
+// never overflows: sigmoid(g) = r for g >= 0 and t * r for g < 0, with r the
+// hardware reciprocal approximation of 1 + t in [1, 2] (rcp.approx, within
+// one float32 ulp).  The product is a few float32 ulps from the exact value
+// wherever it is a normal float32.  Then the 1x128 quantiser on the BF16 h,
+// bit for bit.  Layout and tiling as the activation quantiser:
+// grid x over pairs of 128-channel groups of h, y over 32-row tiles; an
+// eight-lane team per row and group, 16 channels per lane.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  const float t = expf(-fabsf(g));
+  const float r = rcp_approx(__fadd_rn(1.0f, t));
+  const float sig = g >= 0.0f ? r : __fmul_rn(t, r);
+  return __fmul_rn(__fmul_rn(g, sig), u);
+}
+
 __device__ __forceinline__ uint32_t swiglu_pair(uint32_t g2, uint32_t u2) {
-  const float g0 = bf16lo_to_f32(g2), g1 = bf16hi_to_f32(g2);
-  const float u0 = bf16lo_to_f32(u2), u1 = bf16hi_to_f32(u2);
-  const float h0 = __fmul_rn(__fdiv_rn(g0, __fadd_rn(1.0f, expf(-g0))), u0);
-  const float h1 = __fmul_rn(__fdiv_rn(g1, __fadd_rn(1.0f, expf(-g1))), u1);
-  const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(silu_mul(bf16lo_to_f32(g2), bf16lo_to_f32(u2)),
+                                                 silu_mul(bf16hi_to_f32(g2), bf16hi_to_f32(u2)));
   return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
+  return make_uint4(swiglu_pair(g.x, u.x), swiglu_pair(g.y, u.y), swiglu_pair(g.z, u.z), swiglu_pair(g.w, u.w));
 }
 
 template <int U>
 __global__ void __launch_bounds__(256) swiglu_quant_kernel(const uint4* __restrict__ gu, int64_t M, int64_t FB,
-                                                           int64_t ld_v, uint2* __restrict__ q, int64_t ldq_v,
+                                                           int64_t ld_v, uint4* __restrict__ q, int64_t ldq_v,
                                                            float* __restrict__ sa, int64_t ld_sa,
                                                            uint4* __restrict__ h_out, int64_t ldh_v) {
-  const int lane16 = threadIdx.x & 15;
-  const int hh = threadIdx.x >> 4;
+  const int lane8 = threadIdx.x & 7;
+  const int r = threadIdx.x >> 3;  // 32 rows per CTA
   const int64_t fb0 = static_cast<int64_t>(blockIdx.x) * U;
-  const int64_t tiles_m = (M + 15) / 16;
+  const int64_t tiles_m = (M + 31) / 32;
   const int64_t up_off = FB * 16;  // the up half starts F channels (FB * 16 vectors) in
   for (int64_t tm = blockIdx.y; tm < tiles_m; tm += gridDim.y) {
-    const int64_t row = tm * 16 + hh;
+    const int64_t row = tm * 32 + r;
     const bool row_ok = row < M;
-    const uint4* src = gu + row * ld_v + fb0 * 16 + lane16;
-    uint4 gv[U], uv[U];
+    const uint4* src = gu + row * ld_v + fb0 * 16 + lane8 * 2;
+    uint4 gv[U][2], uv[U][2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      gv[u] = uv[u] = make_uint4(0u, 0u, 0u, 0u);
+      gv[u][0] = gv[u][1] = uv[u][0] = uv[u][1] = make_uint4(0u, 0u, 0u, 0u);
       if (row_ok && fb0 + u < FB) {
-        gv[u] = ld_nc_v4(src + u * 16);
-        uv[u] = ld_nc_v4(src + up_off + u * 16);
+        gv[u][0] = ld_nc_v4(src + u * 16);
+        gv[u][1] = ld_nc_v4(src + u * 16 + 1);
+        uv[u][0] = ld_nc_v4(src + up_off + u * 16);
+        uv[u][1] = ld_nc_v4(src + up_off + u * 16 + 1);
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const uint4 h = make_uint4(swiglu_pair(gv[u].x, uv[u].x), swiglu_pair(gv[u].y, uv[u].y),
-                                 swiglu_pair(gv[u].z, uv[u].z), swiglu_pair(gv[u].w, uv[u].w));
-      uint32_t m = absmax8_pairs(h);
+      const uint4 h0 = swiglu8(gv[u][0], uv[u][0]), h1 = swiglu8(gv[u][1], uv[u][1]);
+      uint32_t m = max_pairs(absmax8_pairs(h0), absmax8_pairs(h1));
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
+      for (int off = 4; off > 0; off >>= 1) m = max_pairs(m, __shfl_xor_sync(0xffffffffu, m, off));
       const GroupScale g = group_scale(pairs_to_max(m));
       const int64_t fb = fb0 + u;
       if (row_ok && fb < FB) {
-        q[row * ldq_v + fb * 16 + lane16] = quantise8(h, g);
-        if (lane16 == 0) sa[fb * ld_sa + row] = g.s;
-        if (h_out != nullptr) h_out[row * ldh_v + fb * 16 + lane16] = h;
+        const uint2 c0 = quantise8(h0, g), c1 = quantise8(h1, g);
+        q[row * ldq_v + fb * 8 + lane8] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+        if (lane8 == 0) sa[fb * ld_sa + row] = g.s;
+        if (h_out != nullptr) {
+          uint4* hd = h_out + row * ldh_v + fb * 16 + lane8 * 2;
+          hd[0] = h0;
+          hd[1] = h1;
+        }
       }
     }
   }
@@ -325,11 +350,11 @@ cudaError_t launch_swiglu_quant_act_1x128(const DeviceInfo& dev, const void* gat
   (void)dev;
   constexpr int kUnroll = 2;
   const int64_t FB = F / 128;
-  const int64_t tiles_m = (M + 15) / 16;
+  const int64_t tiles_m = (M + 31) / 32;
   const dim3 grid(static_cast<unsigned>((FB + kUnroll - 1) / kUnroll),
                   static_cast<unsigned>(tiles_m < kMaxGridY ? tiles_m : kMaxGridY));
   swiglu_quant_kernel<kUnroll><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(gate_up), M, FB, ld / 8,
-                                                         static_cast<uint2*>(q), ldq / 8, sa, ld_sa,
+                                                         static_cast<uint4*>(q), ldq / 16, sa, ld_sa,
                                                          static_cast<uint4*>(h), ldh / 8);
   return cudaGetLastError();
 }

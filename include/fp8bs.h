@@ -243,7 +243,10 @@ fp8bs_status fp8bs_e5m6_decode_bf16(const void* codes_u16, int64_t n, void* y_bf
 /*
  * SwiGLU fused with 1x128 quantisation.  gate_up : [M, 2F] BF16 (row stride
  * ld): gate in columns [0, F), up projection in [F, 2F).
- *   h = bf16_rn(silu(g) * u), silu(g) = g / (1 + exp(-g)) in FP32, and h is
+ *   h = bf16_rn(silu(g) * u), silu(g) = g / (1 + exp(-g)) evaluated in FP32
+ *   as g * sigmoid(g) from exp(-|g|) and a reciprocal of 1 + exp(-|g|)
+ *   (within a few FP32 ulps of the exact value wherever that is a normal
+ *   FP32 number, before the BF16 rounding), and h is
  *   quantised exactly as fp8_quant_act_1x128 would: qa [M, F] codes (stride
  *   ldq), sa [F/128, ld_sa] scales.  h itself is written to h_bf16 (stride
  *   ldh) when h_bf16 is not null.  F % 128 == 0.

@@ -76,12 +76,14 @@ def test_e5m6_every_bf16_value():
     assert np.array_equal(f32(y).astype(np.float64), oracle.e5m6_decode(finite))
 
 
-@pytest.mark.parametrize("M,F", [(1, 128), (130, 256), (1000, 2048), (4096, 2048)])
+@pytest.mark.parametrize("M,F", [(1, 128), (130, 256), (33, 384), (1000, 2048), (4096, 2048)])
 def test_swiglu_quant(M, F):
     g = torch.Generator().manual_seed(M + F)
     gate = torch.randn(M, F, generator=g) * 3.0
     up = torch.randn(M, F, generator=g)
-    gate[0, :4] = torch.tensor([0.0, -120.0, 95.0, -0.0])
+    # zeros, huge |g| (exp(-g) overflows float32 for g < -88.7), results near
+    # the bottom of the normal float32 range
+    gate[0, :12] = torch.tensor([0.0, -120.0, 95.0, -0.0, -87.5, -88.5, 88.0, 60.0, -60.0, -30.0, 30.0, -1e-30])
     gu = torch.cat([gate, up], dim=1).to(torch.bfloat16)
     qa, sa, h = fb.fp8_swiglu_quant_act_1x128(gu.to(DEV), return_h=True)
     qa2, sa2 = fb.fp8_swiglu_quant_act_1x128(gu.to(DEV))
