@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config up|down|grouped|decode|tiny]
                     [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+    python bench.py --rows [--only TEXT] [--no-cpu-baseline]   (each kernel alone)
 
 One step is one pass of the whole hot path over one batch of synthetic input
 already resident in HBM:
@@ -605,14 +606,17 @@ def run_rows(args):
 
     lines = []
 
-    def emit(row, what, ms, work, unit, oracle_fn=None, oracle_work=None, oracle_sample=""):
+    def emit(row, what, timer, work, unit, oracle_fn=None, oracle_work=None, oracle_sample=""):
+        if args.only and not any(t in f"{row} {what}" for t in args.only.split("|")):
+            return
+        ms = timer()
         if unit == "GB/s":
             achieved, peak = work / (ms * 1e-3) / 1e9, peaks["hbm_gbs"]
         else:
             achieved, peak = work / (ms * 1e-3) / 1e12, fp8_peak
         line = {"row": row, "workload": what, "us": ms * 1e3, "achieved": achieved, "unit": unit, "peak": peak,
                 "frac": achieved / peak, "peak_source": peak_src, "algorithmic": work}
-        if oracle_fn is not None:
+        if oracle_fn is not None and not args.no_cpu_baseline:
             t = _time_cpu(oracle_fn)
             scale = 1e9 if unit == "GB/s" else 1e12
             line["oracle"] = {"value": oracle_work / t / scale, "unit": unit, "sample": oracle_sample,
@@ -625,20 +629,20 @@ def run_rows(args):
     xs, ws = bf16c(256, K), bf16c(256, K, std=0.02)
     qa, sa = fb.fp8_quant_act_1x128(x)
     qw, sw = fb.fp8_quant_weight_128x128(w)
-    emit("a1 act quant 1x128", f"X [{M},{K}] BF16", _time_kernel(lambda: fb.fp8_quant_act_1x128(x, qa=qa, sa=sa)),
+    emit("a1 act quant 1x128", f"X [{M},{K}] BF16", lambda: _time_kernel(lambda: fb.fp8_quant_act_1x128(x, qa=qa, sa=sa)),
          act_quant_bytes(M, K), "GB/s", lambda: oracle.quant_act_1x128(xs), act_quant_bytes(256, K), "X[:256]")
     emit("a2 weight quant 128x128", f"W [{N},{K}] BF16",
-         _time_kernel(lambda: fb.fp8_quant_weight_128x128(w, qw=qw, sw=sw)), weight_quant_bytes(N, K), "GB/s",
+         lambda: _time_kernel(lambda: fb.fp8_quant_weight_128x128(w, qw=qw, sw=sw)), weight_quant_bytes(N, K), "GB/s",
          lambda: oracle.quant_weight_128x128(ws), weight_quant_bytes(256, K), "W[:256]")
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     qas, sas = oracle.quant_act_1x128(xs[:128])
     qws, sws = oracle.quant_weight_128x128(ws)
     emit("a3-a5 GEMM (BF16 out)", f"up {M}x{N}x{K}",
-         _time_kernel(lambda: fb.fp8_blockscaled_gemm(qa, sa, qw, sw, y=y)), 2 * M * N * K, "TFLOP/s",
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm(qa, sa, qw, sw, y=y)), 2 * M * N * K, "TFLOP/s",
          lambda: oracle.blockscaled_gemm(qas, sas, qws, sws), 2 * 128 * 256 * K, "128 x 256 outputs, full K")
     y32 = torch.empty((M, N), dtype=torch.float32, device=dev)
     emit("NEXT1 GEMM (FP32 out)", f"up {M}x{N}x{K}",
-         _time_kernel(lambda: fb.fp8_blockscaled_gemm(qa, sa, qw, sw, y=y32)), 2 * M * N * K, "TFLOP/s")
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm(qa, sa, qw, sw, y=y32)), 2 * M * N * K, "TFLOP/s")
     del y32
     # down projection
     xd, wd = bf16(M, N), bf16(K, N, std=0.02)
@@ -646,13 +650,13 @@ def run_rows(args):
     qwd, swd = fb.fp8_quant_weight_128x128(wd)
     yd = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     emit("a3-a5 GEMM (BF16 out)", f"down {M}x{K}x{N}",
-         _time_kernel(lambda: fb.fp8_blockscaled_gemm(qad, sad, qwd, swd, y=yd)), 2 * M * N * K, "TFLOP/s")
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm(qad, sad, qwd, swd, y=yd)), 2 * M * N * K, "TFLOP/s")
     # decode
     xdec = bf16(64, K)
     qdec, sdec = fb.fp8_quant_act_1x128(xdec)
     ydec = torch.empty((64, N), dtype=torch.bfloat16, device=dev)
     emit("a7 decode GEMM", f"64x{N}x{K}, W pre-quantised",
-         _time_kernel(lambda: fb.fp8_blockscaled_gemm(qdec, sdec, qw, sw, y=ydec)), gemm_bytes(64, N, K), "GB/s")
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm(qdec, sdec, qw, sw, y=ydec)), gemm_bytes(64, N, K), "GB/s")
     # grouped (MoE): codes and scales drawn directly (the GEMM's inputs)
     cg = workloads.CONFIGS["grouped"]
     routes = torch.multinomial(torch.ones(cg["tokens"], cg["G"]), cg["topk"], replacement=False, generator=gc)
@@ -668,12 +672,12 @@ def run_rows(args):
     swg = torch.rand((Gg, Ng // 128, K // 128), generator=g, device=dev) * 0.01 + 1e-3
     yg = torch.empty((Mg, Ng), dtype=torch.bfloat16, device=dev)
     emit("a6 grouped GEMM", f"{Gg} experts, {Mg} routed rows, N={Ng}, K={K}",
-         _time_kernel(lambda: fb.fp8_blockscaled_grouped_gemm(offsets, Mg, qag, sag, qwg, swg, y=yg)),
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_grouped_gemm(offsets, Mg, qag, sag, qwg, swg, y=yg)),
          2 * Mg * Ng * K, "TFLOP/s")
     del qag, qwg, sag, swg, yg
     # dequant
     wback = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
-    emit("NEXT3 block dequant", f"W [{N},{K}]", _time_kernel(lambda: fb.fp8_dequant_weight_128x128(qw, sw, y=wback)),
+    emit("NEXT3 block dequant", f"W [{N},{K}]", lambda: _time_kernel(lambda: fb.fp8_dequant_weight_128x128(qw, sw, y=wback)),
          N * K + 2 * N * K + 4 * (N // 128) * (K // 128), "GB/s",
          lambda: oracle.dequant_weight_128x128_bf16(qws, sws), 3 * 256 * K, "W[:256]")
     del wback, xd, wd, qad, sad, qwd, swd, yd
@@ -681,37 +685,37 @@ def run_rows(args):
     qt = torch.empty((K, M), dtype=torch.uint8, device=dev)
     st = torch.empty((M // 128, K), dtype=torch.float32, device=dev)
     emit("NEXT2 act quant of X^T", f"X [{M},{K}]",
-         _time_kernel(lambda: fb.fp8_quant_act_1x128_t(x, qt=qt, st=st)), act_quant_bytes(M, K), "GB/s",
+         lambda: _time_kernel(lambda: fb.fp8_quant_act_1x128_t(x, qt=qt, st=st)), act_quant_bytes(M, K), "GB/s",
          lambda: oracle.quant_act_1x128_t(bf16c(256, 1024)), act_quant_bytes(256, 1024), "X[:256, :1024]")
     qwt = torch.empty((K, N), dtype=torch.uint8, device=dev)
     swt = torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev)
     emit("NEXT2 weight code transpose", f"W codes [{N},{K}]",
-         _time_kernel(lambda: fb.fp8_transpose_weight_128x128(qw, sw, qwt=qwt, swt=swt)), 2 * N * K, "GB/s")
+         lambda: _time_kernel(lambda: fb.fp8_transpose_weight_128x128(qw, sw, qwt=qwt, swt=swt)), 2 * N * K, "GB/s")
     dy = bf16(M, N)
     qdy, sdy = fb.fp8_quant_act_1x128(dy)
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     emit("NEXT2 dgrad GEMM", f"dX = dY.W: {M}x{K}x{N}",
-         _time_kernel(lambda: fb.fp8_blockscaled_gemm(qdy, sdy, qwt, swt, y=dx)), 2 * M * N * K, "TFLOP/s")
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm(qdy, sdy, qwt, swt, y=dx)), 2 * M * N * K, "TFLOP/s")
     qdyt, sdyt = fb.fp8_quant_act_1x128_t(dy)
     dw = torch.empty((N, K), dtype=torch.float32, device=dev)
     qat, sat = oracle.quant_act_1x128_t(bf16c(M, 128))
     qbt, sbt = oracle.quant_act_1x128_t(bf16c(M, 256))
     emit("NEXT2 wgrad GEMM (row-scaled, FP32 out)", f"dW = dY^T.X: {N}x{K}x{M}",
-         _time_kernel(lambda: fb.fp8_blockscaled_gemm_rowscaled(qdyt, sdyt, qt, st, y=dw)), 2 * M * N * K,
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm_rowscaled(qdyt, sdyt, qt, st, y=dw)), 2 * M * N * K,
          "TFLOP/s", lambda: oracle.blockscaled_gemm_rowscaled(qat, sat, qbt, sbt), 2 * 128 * 256 * M,
          "128 x 256 outputs, full token range")
     del qt, st, qwt, swt, dy, qdy, sdy, dx, qdyt, sdyt, dw
     # variants
     qpt = torch.empty((M, K), dtype=torch.uint8, device=dev)
     spt = torch.empty((M,), dtype=torch.float32, device=dev)
-    emit("NEXT4 per-token quant", f"X [{M},{K}]", _time_kernel(lambda: fb.fp8_quant_per_token(x, q=qpt, s=spt)),
+    emit("NEXT4 per-token quant", f"X [{M},{K}]", lambda: _time_kernel(lambda: fb.fp8_quant_per_token(x, q=qpt, s=spt)),
          3 * M * K + 4 * M, "GB/s", lambda: oracle.quant_per_token(xs), 3 * 256 * K, "X[:256]")
     spc = torch.empty((K,), dtype=torch.float32, device=dev)
     emit("NEXT4 per-channel quant", f"X [{M},{K}] (read twice)",
-         _time_kernel(lambda: fb.fp8_quant_per_channel(x, q=qpt, s=spc)), 3 * M * K + 4 * K, "GB/s",
+         lambda: _time_kernel(lambda: fb.fp8_quant_per_channel(x, q=qpt, s=spc)), 3 * M * K + 4 * K, "GB/s",
          lambda: oracle.quant_per_channel(xs), 3 * 256 * K, "X[:256]")
     codes = torch.empty((M, K), dtype=torch.int16, device=dev)
-    emit("NEXT4 E5M6 encode", f"X [{M},{K}]", _time_kernel(lambda: fb.e5m6_encode(x, codes=codes)), 4 * M * K,
+    emit("NEXT4 E5M6 encode", f"X [{M},{K}]", lambda: _time_kernel(lambda: fb.e5m6_encode(x, codes=codes)), 4 * M * K,
          "GB/s", lambda: oracle.e5m6_encode_rne_satfinite(xs), 4 * 256 * K, "X[:256]")
     del codes, qpt, spt, spc
     F = N
@@ -720,7 +724,7 @@ def run_rows(args):
     sh = torch.empty((F // 128, M), dtype=torch.float32, device=dev)
     gus = bf16c(128, 2 * F, std=2.0)
     emit("NEXT4 SwiGLU + 1x128 quant", f"gate|up [{M},{2 * F}] -> [{M},{F}]",
-         _time_kernel(lambda: fb.fp8_swiglu_quant_act_1x128(gu, qa=qh, sa=sh)),
+         lambda: _time_kernel(lambda: fb.fp8_swiglu_quant_act_1x128(gu, qa=qh, sa=sh)),
          4 * M * F + M * F + 4 * M * (F // 128), "GB/s", lambda: oracle.swiglu_quant_act_1x128(gus),
          5 * 128 * F, "rows[:128]")
     return lines
@@ -829,6 +833,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", action="store_true",
                     help="time every scope-table kernel on its own (one JSON line per row) and exit")
+    ap.add_argument("--only", default="",
+                    help="with --rows: time only the rows whose name or workload contains this text "
+                         "(alternatives separated by '|')")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps; the number is not a valid measurement", file=sys.stderr)

@@ -130,41 +130,51 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
 
 // ---------------------------------------------------------------------------
 // 128x128 code blocks of W [N, K] -> W^T [K, N], and the block-scale matrix
-// transposed.  One CTA per block: 16-byte loads into shared memory (row
-// stride padded to 144 bytes), then thread t assembles output row t / 2, bytes
-// 64 (t % 2) .. + 63, from one column of the staged block.
+// transposed.  One CTA per block: 16-byte loads into shared memory, then
+// thread t takes the input columns 4 (t % 32) .. + 3 over the 16 rows
+// 16 (t / 32) .., reading 4x4 byte squares with 32-bit loads and transposing
+// them with byte permutes; each of its 4 output rows leaves as one 16-byte run.
 // ---------------------------------------------------------------------------
-constexpr int kPad = 144;
-
 __global__ void __launch_bounds__(256) transpose_weight_128x128_kernel(const uint4* __restrict__ q, int64_t NB,
                                                                        int64_t KB, int64_t ldq_v,
                                                                        const float* __restrict__ sw,
                                                                        uint4* __restrict__ qt, int64_t ldqt_v,
                                                                        float* __restrict__ swt) {
-  __shared__ __align__(16) uint8_t blk[128 * kPad];
+  __shared__ __align__(16) uint8_t blk[128 * 128];
   const int64_t kb = blockIdx.x;
+  const int cg = threadIdx.x & 31;  // input columns 4 cg .. 4 cg + 3 = output rows
+  const int rg = threadIdx.x >> 5;  // input rows 16 rg .. 16 rg + 15 = output columns
   for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
+    uint4 v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int idx = threadIdx.x + 256 * i;  // 1024 chunks of 16 bytes
-      const int row = idx >> 3, ch = idx & 7;
-      *reinterpret_cast<uint4*>(blk + row * kPad + ch * 16) = ld_nc_v4(q + (nb * 128 + row) * ldq_v + kb * 8 + ch);
+      v[i] = ld_nc_v4(q + (nb * 128 + (idx >> 3)) * ldq_v + kb * 8 + (idx & 7));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = threadIdx.x + 256 * i;
+      *reinterpret_cast<uint4*>(blk + (idx >> 3) * 128 + (idx & 7) * 16) = v[i];
     }
     __syncthreads();
-    const int j = threadIdx.x >> 1;         // output row within the block (= input column)
-    const int i0 = (threadIdx.x & 1) * 64;  // first input row gathered
-    uint4* dst = qt + (kb * 128 + j) * ldqt_v + nb * 8 + (threadIdx.x & 1) * 4;
+    uint32_t o[4][4];  // o[c][w]: output row 4 cg + c, bytes of input rows 16 rg + 4 w .. + 3
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint8_t* src = blk + (16 * rg + 4 * w) * 128 + 4 * cg;
+      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(src);
+      const uint32_t a1 = *reinterpret_cast<const uint32_t*>(src + 128);
+      const uint32_t a2 = *reinterpret_cast<const uint32_t*>(src + 256);
+      const uint32_t a3 = *reinterpret_cast<const uint32_t*>(src + 384);
+      const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
+      const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
+      o[0][w] = __byte_perm(t0, t2, 0x5410);
+      o[1][w] = __byte_perm(t0, t2, 0x7632);
+      o[2][w] = __byte_perm(t1, t3, 0x5410);
+      o[3][w] = __byte_perm(t1, t3, 0x7632);
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = i0 + 16 * c + 4 * e;
-        w[e] = static_cast<uint32_t>(blk[i * kPad + j]) | (static_cast<uint32_t>(blk[(i + 1) * kPad + j]) << 8) |
-               (static_cast<uint32_t>(blk[(i + 2) * kPad + j]) << 16) |
-               (static_cast<uint32_t>(blk[(i + 3) * kPad + j]) << 24);
-      }
-      dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+      qt[(kb * 128 + 4 * cg + c) * ldqt_v + nb * 8 + rg] = make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
     }
     if (threadIdx.x == 0) swt[kb * NB + nb] = sw[nb * KB + kb];
     __syncthreads();  // blk is refilled for the next block of this CTA
