@@ -79,6 +79,21 @@ const DeviceInfo* current_device_info(cudaError_t* err) {
     slot.info.status = static_cast<unsigned*>(addr);
     const unsigned zero = 0;
     if (slot.err == cudaSuccess) slot.err = cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    slot.info.workspace_pool = nullptr;
+    if (slot.err == cudaSuccess) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t pool = nullptr;
+      if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+        cuuint64_t keep = ~static_cast<cuuint64_t>(0);
+        (void)cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        slot.info.workspace_pool = pool;
+      } else {
+        (void)cudaGetLastError();  // no pool: GEMM tails run unsplit
+      }
+    }
   });
   if (slot.err != cudaSuccess) {
     *err = slot.err;

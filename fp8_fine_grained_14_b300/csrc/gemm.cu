@@ -89,7 +89,30 @@ struct Params {
   int32_t G;
   unsigned* status;
   uint64_t timeout_ns;
+  // Dense split-K tail: work items 0 .. t_full - 1 are whole tiles; the
+  // remaining tiles are cut into `split` K slices each (items t_full .. n_items
+  // - 1), whose FP32 partial accumulators go to ws and are summed by
+  // split_tail_reduce_kernel.  split == 1: every item is a whole tile.
+  int32_t n_items;
+  int32_t t_full;
+  int32_t split;
+  float* ws;
 };
+
+// Origin of dense cluster tile `tile` (see TileWalker for the order).
+template <int BN, int CM>
+__device__ __forceinline__ void dense_tile_origin(const Params& p, int64_t tile, int32_t rank, int32_t& a_row,
+                                                  int32_t& n0) {
+  const int32_t n_tiles = p.N / BN;
+  const int32_t m_groups = ((p.M + BM - 1) / BM + CM - 1) / CM;
+  // M-fastest keeps a wave on a few weight column tiles and streams A, which
+  // stays L2-resident when it is the smaller operand; otherwise walk
+  // N-fastest so the smaller B is the one re-read from L2
+  const int32_t mg = static_cast<int32_t>(p.n_fastest ? tile / n_tiles : tile % m_groups);
+  const int32_t nt = static_cast<int32_t>(p.n_fastest ? tile % n_tiles : tile / m_groups);
+  a_row = (mg * CM + rank) * BM;
+  n0 = nt * BN;
+}
 
 // Shared-memory layout.  Stage s holds its A tile at a_off(s) and its share
 // of the B tile at b_off(s).  HALF_A (M <= 64): only 64 rows of A are loaded
@@ -153,21 +176,28 @@ struct TileWalker {
     g_row1 = r1;
     g_mgroups = ((r1 - r0 + BM - 1) / BM + CM - 1) / CM;
   }
-  // Returns false when this CTA has no more tiles.
-  __device__ bool get(int32_t& a_row, int32_t& row_end, int32_t& b_row, int32_t& n0, int32_t& group) {
+  // Returns false when this CTA has no more work items.  [kb0, kb1) is the
+  // item's range of K chunks; unit >= 0 numbers a split-K unit of the tail.
+  __device__ bool get(int32_t& a_row, int32_t& row_end, int32_t& b_row, int32_t& n0, int32_t& group, int32_t& kb0,
+                      int32_t& kb1, int32_t& unit) {
     const int64_t t = next;
     next += stride;
+    kb0 = 0;
+    kb1 = p.KB;
+    unit = -1;
     if (!GROUPED) {
-      const int32_t m_groups = ((p.M + BM - 1) / BM + CM - 1) / CM;
-      if (t >= static_cast<int64_t>(m_groups) * n_tiles) return false;
-      // M-fastest keeps a wave on a few weight column tiles and streams A,
-      // which stays L2-resident when it is the smaller operand; otherwise
-      // walk N-fastest so the smaller B is the one re-read from L2
-      const int32_t mg = static_cast<int32_t>(p.n_fastest ? t / n_tiles : t % m_groups);
-      const int32_t nt = static_cast<int32_t>(p.n_fastest ? t % n_tiles : t / m_groups);
-      a_row = (mg * CM + rank) * BM;
+      if (t >= p.n_items) return false;
+      int64_t tile = t;
+      if (t >= p.t_full) {
+        const int32_t u = static_cast<int32_t>(t - p.t_full);
+        const int32_t slice = u % p.split;
+        tile = p.t_full + u / p.split;
+        kb0 = slice * p.KB / p.split;
+        kb1 = (slice + 1) * p.KB / p.split;
+        unit = u;
+      }
+      dense_tile_origin<BN, CM>(p, tile, rank, a_row, n0);
       row_end = p.M;
-      n0 = nt * BN;
       b_row = n0;
       group = 0;
       return true;
@@ -269,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tempty_base = CG > 1 ? map_shared_rank(bar_tempty, 0) : bar_tempty;
 
   TileWalker<GROUPED, BN, CG> tiles(p, rank);
-  int32_t a_row, row_end, b_row, n0, group;
+  int32_t a_row, row_end, b_row, n0, group, kb0, kb1, unit;
 
   if (warp < kFirstEpiWarp) {
     // 128 FP32 accumulators per promotion thread (BN = 256) need more than the
@@ -280,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;  // per stage: ever issued / parity of last issue
       bool ok = true;
-      while (ok && tiles.get(a_row, row_end, b_row, n0, group)) {
-        for (int kb = 0; kb < p.KB; ++kb) {
+      while (ok && tiles.get(a_row, row_end, b_row, n0, group, kb0, kb1, unit)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns)) {
             abort_cta(abort_flag, p.status);
             ok = false;
@@ -329,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
       uint32_t committed = 0, committed_parity = 0;  // per TMEM buffer: ever committed / parity of last commit
       bool ok = true;
-      while (ok && tiles.get(a_row, row_end, b_row, n0, group)) {
-        for (int kb = 0; kb < p.KB; ++kb) {
+      while (ok && tiles.get(a_row, row_end, b_row, n0, group, kb0, kb1, unit)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           // (with a pair, the peer's promotion warps also release the buffer)
           const bool drained = CG == 1 ? mbar_wait(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag, p.timeout_ns)
                                        : mbar_wait_cluster(bar_tempty + 8 * buf, bphase ^ 1u, abort_flag,
@@ -387,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t buf = 0, bphase = 0;
     bool ok = true;
     const bool live = !HALF_A || q < 2;  // the warp's TMEM lanes can hold output rows
-    while (ok && tiles.get(a_row, row_end, b_row, n0, group)) {
+    while (ok && tiles.get(a_row, row_end, b_row, n0, group, kb0, kb1, unit)) {
       const int32_t row = a_row + q * 32 + lane;  // this thread's output row
       const bool row_ok = row < row_end;
       // rows past the end read a valid row's scale and drop the result
@@ -409,22 +439,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       float cs_next[kColVec];
       if (RS) {
 #pragma unroll
-        for (int v = 0; v < kColVec; ++v) colscale[lane * kColVec + v] = __ldg(sb_col + v);
-        const int k1 = p.KB > 1 ? 1 : 0;
+        for (int v = 0; v < kColVec; ++v)
+          colscale[lane * kColVec + v] = __ldg(sb_col + static_cast<int64_t>(kb0) * p.ld_sb + v);
+        const int k1 = kb0 + 1 < kb1 ? kb0 + 1 : kb0;
 #pragma unroll
         for (int v = 0; v < kColVec; ++v) cs_next[v] = __ldg(sb_col + static_cast<int64_t>(k1) * p.ld_sb + v);
         __syncwarp();
       }
 
-      float sa_next = __ldg(sa_col);
-      float sw_next = RS ? 1.0f : __ldg(sw_row);
-      for (int kb = 0; kb < p.KB; ++kb) {
+      float sa_next = __ldg(sa_col + static_cast<int64_t>(kb0) * p.ld_sa);
+      float sw_next = RS ? 1.0f : __ldg(sw_row + kb0);
+      for (int kb = kb0; kb < kb1; ++kb) {
         const float scale = sa_next * sw_next * row_mask;
         const float2 scale2 = make_float2(scale, scale);
-        const int kn = kb + 1 < p.KB ? kb + 1 : kb;  // prefetch the next chunk's scales
+        const int kn = kb + 1 < kb1 ? kb + 1 : kb;  // prefetch the next chunk's scales
         sa_next = __ldg(sa_col + static_cast<int64_t>(kn) * p.ld_sa);
         if (!RS) sw_next = __ldg(sw_row + kn);
-        const float* cs = colscale + (kb & 1) * kHalfCols;  // this chunk's column scales (RS)
+        const float* cs = colscale + ((kb - kb0) & 1) * kHalfCols;  // this chunk's column scales (RS)
         const bool waited = mbar_wait(bar_tfull + 8 * buf, bphase, abort_flag, p.timeout_ns);
         if (!__all_sync(0xffffffffu, waited)) {
           abort_cta(abort_flag, p.status);
@@ -482,8 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // chunk kb - 1) and fetch the one after
           __syncwarp();
 #pragma unroll
-          for (int v = 0; v < kColVec; ++v) colscale[((kb + 1) & 1) * kHalfCols + lane * kColVec + v] = cs_next[v];
-          const int k2 = kb + 2 < p.KB ? kb + 2 : p.KB - 1;
+          for (int v = 0; v < kColVec; ++v)
+            colscale[((kb - kb0 + 1) & 1) * kHalfCols + lane * kColVec + v] = cs_next[v];
+          const int k2 = kb + 2 < kb1 ? kb + 2 : kb1 - 1;
 #pragma unroll
           for (int v = 0; v < kColVec; ++v) cs_next[v] = __ldg(sb_col + static_cast<int64_t>(k2) * p.ld_sb + v);
           __syncwarp();
@@ -492,6 +524,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (buf == 0) bphase ^= 1u;
       }
       if (!ok) break;
+
+      if (!GROUPED && unit >= 0) {
+        // split-K unit of a tail tile: this warp's FP32 partial (32 rows x
+        // kHalfCols) to the workspace, float4 j of lane l at j * 32 + l so that
+        // each store instruction covers 512 contiguous bytes
+        float4* part = reinterpret_cast<float4*>(p.ws) +
+                       ((static_cast<int64_t>(unit) * CG + rank) * kEpiWarps + epi) * (8 * kHalfCols) + lane;
+#pragma unroll
+        for (int j = 0; j < kHalfCols / 4; ++j)
+          part[j * 32] = make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y);
+        continue;
+      }
 
       // ---- epilogue: BF16 (RNE) or FP32, swizzled staging, store ----
 #pragma unroll
@@ -566,6 +610,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Split-K tail: sums the FP32 partials of each tail tile in slice order (the
+// result does not depend on which unit finished first) and writes Y.  One CTA
+// per (tail tile, CTA rank of the tile, promotion-warp region of 32 rows x
+// BN / 2 columns); thread t sums float4 columns t / 32, t / 32 + 8, .. of row
+// t % 32.
+template <int BN, int CG, bool F32>
+__global__ void __launch_bounds__(256) split_tail_reduce_kernel(const Params p) {
+  constexpr int kHalfCols = BN / 2;
+  constexpr int64_t kRegion = 8 * kHalfCols;  // float4 per warp region
+  const int32_t region = static_cast<int32_t>(blockIdx.x % kEpiWarps);
+  const int32_t rank = static_cast<int32_t>((blockIdx.x / kEpiWarps) % CG);
+  const int32_t tail = static_cast<int32_t>(blockIdx.x / (kEpiWarps * CG));
+  int32_t a_row, n0;
+  dense_tile_origin<BN, CG>(p, static_cast<int64_t>(p.t_full) + tail, rank, a_row, n0);
+  const int lane = threadIdx.x & 31;
+  const int32_t row = a_row + (region & 3) * 32 + lane;
+  const int32_t col0 = n0 + (region >> 2) * kHalfCols;
+  const int64_t slice_stride = static_cast<int64_t>(CG) * kEpiWarps * kRegion;
+  const float4* part = reinterpret_cast<const float4*>(p.ws) +
+                       ((static_cast<int64_t>(tail) * p.split * CG + rank) * kEpiWarps + region) * kRegion + lane;
+  for (int j = threadIdx.x >> 5; j < kHalfCols / 4; j += 8) {
+    float4 sum = __ldcg(part + j * 32);
+    for (int sl = 1; sl < p.split; ++sl) {
+      const float4 v = __ldcg(part + sl * slice_stride + j * 32);
+      sum.x = __fadd_rn(sum.x, v.x);
+      sum.y = __fadd_rn(sum.y, v.y);
+      sum.z = __fadd_rn(sum.z, v.z);
+      sum.w = __fadd_rn(sum.w, v.w);
+    }
+    if (row < p.M) {
+      const int64_t off = static_cast<int64_t>(row) * p.ldy + col0 + 4 * j;
+      if (F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.y) + off) = sum;
+      } else {
+        const __nv_bfloat162 lo = __float22bfloat162_rn(make_float2(sum.x, sum.y));
+        const __nv_bfloat162 hi = __float22bfloat162_rn(make_float2(sum.z, sum.w));
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.y) + off) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      }
+    }
+  }
+}
+
 // Largest number of clusters of this kernel variant that can be resident at
 // once on the current device (queried once per device and variant).
 template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A>
@@ -589,9 +676,19 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
 
 // Persistent launch: one cluster of CG CTAs per CG SMs, at most one per
 // cluster tile.
+// Smallest K slice of a split tail tile, in 128-K chunks.
+constexpr int kMinSplitChunks = 4;
+
+// Persistent launch: one cluster of CG CTAs per CG SMs, at most one per work
+// item.  When the dense tiles leave a last round that fills at most half of the
+// resident clusters, those tail tiles are split along K over the idle
+// clusters (FP32 partials in a workspace: `scratch` when given, else
+// stream-ordered memory from the library's per-device pool) and summed by
+// split_tail_reduce_kernel.
 template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false>
 cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                          const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream) {
+                          const CUtensorMap& tmY, const Params& p0, int64_t cluster_tiles, cudaStream_t stream,
+                          float* scratch, size_t scratch_bytes) {
   using L = Smem<BN, STAGES, CG, RS, HALF_A>;
   auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>;
   if (BN == 256) {
@@ -617,9 +714,52 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(CG, 1, 1);
   const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>(dev, cfg);
-  const int64_t clusters = cluster_tiles < resident ? cluster_tiles : resident;
+  Params p = p0;
+  p.n_items = static_cast<int32_t>(cluster_tiles);
+  p.t_full = static_cast<int32_t>(cluster_tiles);
+  p.split = 1;
+  p.ws = nullptr;
+  bool owned = false;
+  if constexpr (!GROUPED) {
+    const int64_t tail = cluster_tiles % resident;
+    if (cluster_tiles > resident && tail > 0 && 2 * tail <= resident) {
+      int64_t split = resident / tail;
+      if (split > p.KB / kMinSplitChunks) split = p.KB / kMinSplitChunks;
+      const size_t bytes = static_cast<size_t>(tail * split) * CG * BM * BN * sizeof(float);
+      float* ws = nullptr;
+      if (split >= 2) {
+        if (scratch != nullptr) {
+          if (bytes > scratch_bytes) return cudaErrorInvalidValue;
+          ws = scratch;
+        } else if (dev.workspace_pool != nullptr &&
+                   cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), bytes, dev.workspace_pool, stream) ==
+                       cudaSuccess) {
+          owned = true;
+        } else {
+          (void)cudaGetLastError();  // no workspace: run the tail tiles whole
+          ws = nullptr;
+        }
+      }
+      if (ws != nullptr) {
+        p.ws = ws;
+        p.split = static_cast<int32_t>(split);
+        p.t_full = static_cast<int32_t>(cluster_tiles - tail);
+        p.n_items = static_cast<int32_t>(p.t_full + tail * split);
+      }
+    }
+  }
+  const int64_t clusters = p.n_items < resident ? p.n_items : resident;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
   e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmY, p);
+  if (e == cudaSuccess && p.split > 1) {
+    const unsigned blocks = static_cast<unsigned>((p.n_items - p.t_full) / p.split) * CG * kEpiWarps;
+    split_tail_reduce_kernel<BN, CG, F32><<<blocks, 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  if (owned) {
+    const cudaError_t f = cudaFreeAsync(p.ws, stream);
+    if (e == cudaSuccess) e = f;
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -670,22 +810,23 @@ enum class Shape { kNarrow, kNarrowHalfA, kWide, kPair };
 
 template <bool GROUPED, bool F32, bool RS = false>
 cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                         const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream) {
+                         const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream,
+                         float* scratch = nullptr, size_t scratch_bytes = 0) {
   switch (shape) {
     case Shape::kNarrow:
-      return launch_kernel<128, RS ? kStages128RS : kStages128, GROUPED, 1, F32, RS>(dev, tmA, tmB, tmY, p,
-                                                                                      cluster_tiles, stream);
+      return launch_kernel<128, RS ? kStages128RS : kStages128, GROUPED, 1, F32, RS>(
+          dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
     case Shape::kNarrowHalfA:
       if constexpr (!GROUPED && !RS)
         return launch_kernel<128, kStages128HalfA, false, 1, F32, false, true>(dev, tmA, tmB, tmY, p, cluster_tiles,
-                                                                             stream);
+                                                                             stream, scratch, scratch_bytes);
       return cudaErrorInvalidValue;
     case Shape::kWide:
-      return launch_kernel<256, RS ? kStages256RS : kStages256, GROUPED, 1, F32, RS>(dev, tmA, tmB, tmY, p,
-                                                                                      cluster_tiles, stream);
+      return launch_kernel<256, RS ? kStages256RS : kStages256, GROUPED, 1, F32, RS>(
+          dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
     case Shape::kPair:
-      return launch_kernel<256, RS ? kStagesPairRS : kStagesPair, GROUPED, 2, F32, RS>(dev, tmA, tmB, tmY, p,
-                                                                                        cluster_tiles, stream);
+      return launch_kernel<256, RS ? kStagesPairRS : kStagesPair, GROUPED, 2, F32, RS>(
+          dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
   }
   return cudaErrorInvalidValue;
 }
@@ -694,7 +835,8 @@ cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& 
 
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
-                                    int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+                                    int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                                    float* scratch, size_t scratch_bytes) {
   // Wide tiles (BN = 256) halve the operand traffic per FLOP; narrow ones keep
   // every SM busy when there are few tiles (skinny, decode-shaped M).
   const int64_t m_tiles = (M + BM - 1) / BM;
@@ -713,8 +855,9 @@ cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64
     return cudaErrorInvalidValue;
   const Params p = make_params(dev, sa, ld_sa, sw, y, ldy, M, N, K, nullptr, 1);
   const int64_t cluster_tiles = (m_tiles + CG - 1) / CG * (N / BN);
-  return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream)
-               : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream);
+  return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes)
+               : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch,
+                                            scratch_bytes);
 }
 
 cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,

@@ -13,6 +13,10 @@ struct DeviceInfo {
   int num_sms;
   int max_smem_optin;
   unsigned* status;  // device address of this device's status word
+  // Library-owned stream-ordered memory pool for GEMM workspaces (split-K
+  // partials).  It keeps freed memory for reuse instead of returning it at
+  // every synchronisation; null when the device offers no memory pools.
+  cudaMemPool_t workspace_pool;
 };
 
 // Per-device facts, looked up once per device (thread-safe).  Returns nullptr
@@ -33,9 +37,14 @@ cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, in
 
 // Returns cudaErrorInvalidValue when a tensor map cannot be encoded.
 // y is BF16 (y_f32 false) or FP32 (y_f32 true); ldy in elements of that type.
+// When the last round of tiles would leave most SMs idle, the tail tiles are
+// split along K; their FP32 partials go to `scratch` (scratch_bytes long; the
+// launch fails with cudaErrorInvalidValue if it is too small) or, when scratch
+// is null, to stream-ordered memory from DeviceInfo::workspace_pool.
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
-                                    int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+                                    int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                                    float* scratch = nullptr, size_t scratch_bytes = 0);
 
 cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,
                                             int64_t M_total, const void* qa, int64_t ldqa, const float* sa,

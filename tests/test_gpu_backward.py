@@ -126,3 +126,22 @@ def test_wgrad_full_size_sampled():
     assert_codes_equal(u8(qxt), qb_r, "codes of X^T")
     y_ref = oracle.blockscaled_gemm_rowscaled(qa_r, sa_r, qb_r, sb_r)
     assert_gemm_close(f32(dw)[rows], y_ref, what="dW rows")
+
+
+def test_rowscaled_split_tail():
+    """The row-scaled GEMM with a split-K tail (80 pair tiles on 74 resident
+    pairs): every row, the last column tiles, and BF16 == RNE(FP32)."""
+    M, N, K = 2048, 2560, 6144
+    a, b = _rowscaled_case(M, N, K, seed=7)
+    qa, sa = fb.fp8_quant_act_1x128(a.to(DEV))
+    qb, sb = fb.fp8_quant_act_1x128(b.to(DEV))
+    y16 = fb.fp8_blockscaled_gemm_rowscaled(qa, sa, qb, sb)
+    y32 = fb.fp8_blockscaled_gemm_rowscaled(qa, sa, qb, sb, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    cols = np.arange(N - 512, N)
+    qa_r, sa_r = oracle.quant_act_1x128(f32(a))
+    qb_r, sb_r = oracle.quant_act_1x128(f32(b)[cols])
+    y_ref = oracle.blockscaled_gemm_rowscaled(qa_r, sa_r, qb_r, sb_r)
+    assert_gemm_close(f32(y32)[:, cols], y_ref, what="f32")
+    assert np.array_equal(oracle.bf16_round(f32(y32)).view(np.uint32), f32(y16).view(np.uint32))

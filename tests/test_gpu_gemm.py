@@ -175,3 +175,29 @@ def test_f32_output_strided_and_full_size_sampled():
     sub = ybig[torch.as_tensor(rows, device=DEV)][:, torch.as_tensor(cols, device=DEV)]
     assert_gemm_close(f32(sub), y_ref)
     assert np.array_equal(oracle.bf16_round(f32(ybig[:, :N])).view(np.uint32), f32(y16).view(np.uint32))
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 6144), (2148, 2560, 6144)])
+def test_split_tail(M, N, K):
+    """80 (or 90) CTA-pair tiles on 74 resident pairs leave a last round of a
+    few tiles, which the launcher splits along K over the idle SMs and sums in
+    a second kernel.  Every row and the last column tiles (where the tail tiles
+    lie in the M-fastest order) are checked against the oracle; BF16 is the
+    rounding of FP32; repeated launches give identical bits (the slices are
+    summed in a fixed order)."""
+    x, w = workloads.dense_inputs(M, N, K, seed=M + 3 * N + K)
+    xd, wd = x.to(DEV), w.to(DEV)
+    qa, sa = fb.fp8_quant_act_1x128(xd)
+    qw, sw = fb.fp8_quant_weight_128x128(wd)
+    y16 = fb.fp8_blockscaled_gemm(qa, sa, qw, sw)
+    y32 = fb.fp8_blockscaled_gemm(qa, sa, qw, sw, out_dtype=torch.float32)
+    y16b = fb.fp8_blockscaled_gemm(qa, sa, qw, sw)
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    assert torch.equal(y16, y16b)
+    assert np.array_equal(oracle.bf16_round(f32(y32)).view(np.uint32), f32(y16).view(np.uint32))
+    rows = np.arange(M)
+    blocks = [0, 5, N // 128 - 4, N // 128 - 3, N // 128 - 2, N // 128 - 1]
+    _, _, _, _, y_ref, cols = oracle_dense_sampled(x, w, rows, blocks)
+    sub = y32[:, torch.as_tensor(cols, device=DEV)]
+    assert_gemm_close(f32(sub), y_ref)
