@@ -31,6 +31,7 @@ EXPORTS = {
     "fp8_quant_act_1x128": [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
     "fp8_quant_weight_128x128": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
     "fp8_blockscaled_gemm": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
+    "fp8_blockscaled_gemm_noalloc": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_grouped_gemm": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
     "fp8_blockscaled_gemm_f32": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_grouped_gemm_f32": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
@@ -158,6 +159,27 @@ def fp8_blockscaled_gemm(qa, sa, qw, sw, y=None, stream=None, out_dtype=torch.bf
     st = getattr(lib, fn)(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
                           _ptr(y), y.stride(0), M, N, K, _stream(stream))
     _check(fn, st)
+    return y
+
+
+def fp8_blockscaled_gemm_noalloc(qa, sa, qw, sw, y=None, stream=None):
+    """fp8_blockscaled_gemm (BF16 out) with the split-K workspace in the
+    library's fixed static device array instead of its memory pool: the call
+    allocates nothing.  Calls that split share that array, so keep them on
+    one stream."""
+    _require(qa, torch.uint8, "qa", 2)
+    _require(qw, torch.uint8, "qw", 2)
+    _require(sa, torch.float32, "sa", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    _require(y, torch.bfloat16, "y", 2)
+    if not sw.is_contiguous():
+        raise ValueError("sw must be contiguous")
+    st = lib.fp8_blockscaled_gemm_noalloc(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0),
+                                          _ptr(sw), _ptr(y), y.stride(0), M, N, K, _stream(stream))
+    _check("fp8_blockscaled_gemm_noalloc", st)
     return y
 
 

@@ -21,6 +21,13 @@ namespace fp8bs {
 // variable).  Kernels record failures here; fp8bs_last_device_error reads it.
 __device__ unsigned g_status_word;
 
+// Fixed split-K workspace of fp8_blockscaled_gemm_noalloc, one per device:
+// 20 MiB covers the largest split tail on a 148-SM device (a split tail has
+// at most one work unit per resident cluster, each unit 128 rows x 256
+// columns of FP32 per CTA).
+constexpr size_t kGemmScratchBytes = size_t(20) << 20;
+static __device__ __align__(256) unsigned char g_gemm_scratch[kGemmScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -209,7 +216,7 @@ namespace {
 // 4 (FP32 y) and sets the row-stride rule for y.
 fp8bs_status dense_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw, int64_t ldqw,
                         const float* sw, void* y, int64_t ldy, int out_bytes, int64_t M, int64_t N, int64_t K,
-                        cudaStream_t stream, const char* name) {
+                        cudaStream_t stream, const char* name, bool use_static_scratch = false) {
   if (M < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldqw < 0 || ldy < 0) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim)
     return FP8BS_ERR_UNSUPPORTED_SHAPE;
@@ -222,8 +229,21 @@ fp8bs_status dense_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t l
   cudaError_t e;
   const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
   if (dev == nullptr) return cuda_failure("device query", e);
+  float* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  if (use_static_scratch) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, fp8bs::g_gemm_scratch);  // this device's copy
+    if (e != cudaSuccess) return cuda_failure("scratch address", e);
+    scratch = static_cast<float*>(addr);
+    scratch_bytes = fp8bs::kGemmScratchBytes;
+  }
   e = fp8bs::launch_blockscaled_gemm(*dev, qa, ldqa, sa, ld_sa, qw, ldqw, sw, y, ldy, out_bytes == 4, M, N, K,
-                                     stream);
+                                     stream, scratch, scratch_bytes);
+  if (e == cudaErrorMemoryAllocation && use_static_scratch) {
+    std::snprintf(fp8bs::t_detail, sizeof(fp8bs::t_detail), "%s: split-K workspace larger than the static scratch", name);
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  }
   return e == cudaSuccess ? FP8BS_OK : cuda_failure(name, e);
 }
 
@@ -406,6 +426,13 @@ fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa,
                                   int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,
                                   int64_t K, cudaStream_t stream) {
   return dense_gemm(qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, 2, M, N, K, stream, "fp8_blockscaled_gemm launch");
+}
+
+fp8bs_status fp8_blockscaled_gemm_noalloc(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,
+                                          int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,
+                                          int64_t K, cudaStream_t stream) {
+  return dense_gemm(qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, 2, M, N, K, stream,
+                    "fp8_blockscaled_gemm_noalloc launch", true);
 }
 
 fp8bs_status fp8_blockscaled_gemm_f32(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,

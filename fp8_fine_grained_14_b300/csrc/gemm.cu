@@ -729,7 +729,7 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
       float* ws = nullptr;
       if (split >= 2) {
         if (scratch != nullptr) {
-          if (bytes > scratch_bytes) return cudaErrorInvalidValue;
+          if (bytes > scratch_bytes) return cudaErrorMemoryAllocation;
           ws = scratch;
         } else if (dev.workspace_pool != nullptr &&
                    cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), bytes, dev.workspace_pool, stream) ==

@@ -39,7 +39,7 @@ cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, in
 // y is BF16 (y_f32 false) or FP32 (y_f32 true); ldy in elements of that type.
 // When the last round of tiles would leave most SMs idle, the tail tiles are
 // split along K; their FP32 partials go to `scratch` (scratch_bytes long; the
-// launch fails with cudaErrorInvalidValue if it is too small) or, when scratch
+// launch fails with cudaErrorMemoryAllocation if it is too small) or, when scratch
 // is null, to stream-ordered memory from DeviceInfo::workspace_pool.
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,

@@ -256,6 +256,23 @@ fp8bs_status fp8_swiglu_quant_act_1x128(const void* gate_up_bf16, int64_t M, int
                                         void* h_bf16, int64_t ldh, cudaStream_t stream);
 
 /*
+ * fp8_blockscaled_gemm without any allocation.  The pages have no counterpart
+ * of this call: it exists for callers that must not allocate (e.g. inside
+ * graph capture with allocation disabled).  Same arguments, layouts, results
+ * (bit for bit) and error behaviour as fp8_blockscaled_gemm, except that when
+ * the last round of tiles is split along K, the FP32 partials go to a fixed
+ * 20 MiB static device array of the library (one per device) instead of the
+ * library's stream-ordered pool.  That array is shared by every call on the
+ * device, so calls whose tails split must be ordered (one stream, or
+ * synchronised).  Returns FP8BS_ERR_UNSUPPORTED_SHAPE if a problem's split
+ * tail would need more than the array holds (not reachable on 148-SM parts).
+ */
+fp8bs_status fp8_blockscaled_gemm_noalloc(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                          const void* qw, int64_t ldqw, const float* sw,
+                                          void* y_bf16, int64_t ldy,
+                                          int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * Text naming the CUDA error (and the step) behind the last FP8BS_ERR_CUDA
  * returned to the calling host thread; "" if none.  Valid until the thread's
  * next call into the library.
