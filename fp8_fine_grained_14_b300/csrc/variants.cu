@@ -130,6 +130,112 @@ __global__ void __launch_bounds__(256) quant_per_channel_kernel(const uint4* __r
   }
 }
 
+// Per channel in one pass, for M <= kPcCluster * 32 * 16 rows: a cluster of
+// kPcCluster CTAs covers 64 channels and all rows (CTA rank r: rows 32 R r ..
+// 32 R r + 32 R - 1), each thread holding R 16-byte vectors (8 channels of R
+// rows, row phase t / 8) in registers.  Column maxima combine per thread,
+// across the warp's four row phases (shuffles), across the eight warps
+// (shared memory) and across the cluster (each CTA reads every rank's maxima
+// through distributed shared memory after a cluster barrier); then every CTA
+// codes its rows from registers, so X is read once and no atomics are needed.
+constexpr int kPcCluster = 8;
+
+__device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+template <int R>
+__global__ void __launch_bounds__(256) quant_per_channel_cluster_kernel(const uint4* __restrict__ x, int64_t M,
+                                                                        int64_t KV, int64_t ldx_v,
+                                                                        uint2* __restrict__ q, int64_t ldq_v,
+                                                                        float* __restrict__ s) {
+  __shared__ uint32_t warp_max[8][8][4];            // [warp][channel group][BF16 pair]
+  __shared__ __align__(16) uint32_t cta_max[8][4];  // [channel group][BF16 pair]: this CTA's maxima
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int cg = t & 7, rp = t >> 3;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t cb = blockIdx.x / kPcCluster;
+  const int64_t col_v = cb * 8 + cg;
+  const bool col_ok = col_v < KV;
+  const int64_t row0 = static_cast<int64_t>(rank) * (32 * R) + rp;
+  uint4 v[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int64_t row = row0 + 32 * i;
+    v[i] = (col_ok && row < M) ? ld_nc_v4(x + row * ldx_v + col_v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  constexpr uint32_t kMag = 0x7FFF7FFFu;
+  uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    m0 = max_pairs(m0, v[i].x & kMag);
+    m1 = max_pairs(m1, v[i].y & kMag);
+    m2 = max_pairs(m2, v[i].z & kMag);
+    m3 = max_pairs(m3, v[i].w & kMag);
+  }
+#pragma unroll
+  for (int off = 8; off <= 16; off <<= 1) {
+    m0 = max_pairs(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+    m1 = max_pairs(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+    m2 = max_pairs(m2, __shfl_xor_sync(0xffffffffu, m2, off));
+    m3 = max_pairs(m3, __shfl_xor_sync(0xffffffffu, m3, off));
+  }
+  if (lane < 8) {
+    warp_max[warp][lane][0] = m0;
+    warp_max[warp][lane][1] = m1;
+    warp_max[warp][lane][2] = m2;
+    warp_max[warp][lane][3] = m3;
+  }
+  __syncthreads();
+  if (t < 32) {
+    const int c = t >> 2, w = t & 3;
+    uint32_t mm = warp_max[0][c][w];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) mm = max_pairs(mm, warp_max[k][c][w]);
+    cta_max[c][w] = mm;
+  }
+  cluster_sync_all();  // every CTA's maxima visible to the cluster
+  uint32_t a0 = 0u, a1 = 0u, a2 = 0u, a3 = 0u;
+  const uint32_t local = smem_u32(&cta_max[cg][0]);
+#pragma unroll
+  for (int r = 0; r < kPcCluster; ++r) {
+    const uint4 o = ld_shared_cluster_v4(map_shared_rank(local, r));
+    a0 = max_pairs(a0, o.x);
+    a1 = max_pairs(a1, o.y);
+    a2 = max_pairs(a2, o.z);
+    a3 = max_pairs(a3, o.w);
+  }
+  cluster_sync_all();  // no CTA leaves while another may still read its maxima
+  const uint32_t a[4] = {a0, a1, a2, a3};
+  GroupScale g[8];
+  uint32_t special0 = 0u, special1 = 0u;  // zero scales or scales below 2^-64, 0xFF per element
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    g[c] = group_scale((c & 1) ? bf16hi_to_f32(a[c >> 1]) : bf16lo_to_f32(a[c >> 1]));
+    const uint32_t mark = (g[c].s == 0.0f || !g[c].fast) ? 0xFFu : 0u;
+    if (c < 4)
+      special0 |= mark << (8 * c);
+    else
+      special1 |= mark << (8 * (c - 4));
+  }
+  if (col_ok) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int64_t row = row0 + 32 * i;
+      if (row < M) q[row * ldq_v + col_v] = quantise8_cols(v[i], g, special0, special1);
+    }
+    if (rank == 0 && rp == 0) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) s[col_v * 8 + c] = g[c].s;
+    }
+  }
+}
+
 __global__ void channel_scales_kernel(uint32_t* __restrict__ amax_bits_to_scales, int64_t K) {
   const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (k < K) {
@@ -310,10 +416,42 @@ if (KV <= 256)
   return cudaGetLastError();
 }
 
+template <int R>
+cudaError_t launch_per_channel_cluster(const void* x, int64_t M, int64_t KV, int64_t ldx, void* q, int64_t ldq,
+                                       float* s, cudaStream_t stream) {
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = kPcCluster;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((KV + 7) / 8 * kPcCluster), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_per_channel_cluster_kernel<R>, static_cast<const uint4*>(x), M, KV, ldx / 8,
+                            static_cast<uint2*>(q), ldq / 8, s);
+}
+
 cudaError_t launch_quant_per_channel(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
                                      void* q, int64_t ldq, float* s, cudaStream_t stream) {
   (void)dev;
   const int64_t KV = K / 8;
+  // One pass on clusters when every row fits a cluster's registers.
+  cudaError_t e = cudaErrorNotSupported;
+  if (M <= kPcCluster * 32 * 1)
+    e = launch_per_channel_cluster<1>(x, M, KV, ldx, q, ldq, s, stream);
+  else if (M <= kPcCluster * 32 * 2)
+    e = launch_per_channel_cluster<2>(x, M, KV, ldx, q, ldq, s, stream);
+  else if (M <= kPcCluster * 32 * 4)
+    e = launch_per_channel_cluster<4>(x, M, KV, ldx, q, ldq, s, stream);
+  else if (M <= kPcCluster * 32 * 8)
+    e = launch_per_channel_cluster<8>(x, M, KV, ldx, q, ldq, s, stream);
+  else if (M <= kPcCluster * 32 * 16)
+    e = launch_per_channel_cluster<16>(x, M, KV, ldx, q, ldq, s, stream);
+  if (e != cudaErrorNotSupported) return e == cudaSuccess ? cudaGetLastError() : e;
   uint32_t* bits = reinterpret_cast<uint32_t*>(s);
   zero_words_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(bits, K);
   const int64_t row_tiles = (M + 63) / 64;
