@@ -285,16 +285,46 @@ __device__ __forceinline__ uint32_t e5m6_to_bf16(uint32_t c) {
   return sign | (f >> 16);  // exact: the low 16 bits are zero
 }
 
+// Two E5M6 codes (in the two 16-bit halves) from two BF16 values (one 32-bit
+// word), with integer arithmetic on the bit patterns: dropping BF16's last
+// mantissa bit with round-to-nearest-even is (a + kept LSB) >> 1, and the
+// exponent is re-biased from 127 to 15 by subtracting 112 << 6.  Halves above
+// 65024 saturate to 0x7BF; halves below 2^-14 (E5M6 subnormals) go through
+// e5m6_encode one by one.  Per-half flags come from additions that cannot
+// carry into the other half.
+__device__ __forceinline__ uint32_t e5m6_encode2(uint32_t w) {
+  const uint32_t a = w & 0x7FFF7FFFu;
+  const uint32_t rounded = ((a + ((a >> 1) & 0x00010001u)) >> 1) & 0x7FFF7FFFu;
+  uint32_t code = rounded - 0x1C001C00u;
+  const uint32_t small = ~(a + 0x47804780u) & 0x80008000u;  // half < 0x3880 (2^-14)
+  const uint32_t big = (a + 0x38813881u) & 0x80008000u;     // half > 0x477E (65024)
+  const uint32_t big_mask = (big >> 15) * 0xFFFFu;
+  code = (code & ~big_mask) | (0x07BF07BFu & big_mask);
+  if (small != 0u) {
+    // (rare) recompute both halves: the subnormal half's subtraction above
+    // may have borrowed from its neighbour
+    code = e5m6_encode(bf16lo_to_f32(w & 0x7FFF7FFFu)) | (e5m6_encode(bf16hi_to_f32(w & 0x7FFF7FFFu)) << 16);
+  }
+  return code | ((w >> 4) & 0x08000800u);
+}
+
+// Grid-stride over blocks of 1024 vectors: each thread loads its 4 vectors
+// (t, t + 256, ..) of a block before coding any of them.
 __global__ void __launch_bounds__(256) cast_e5m6_kernel(const uint4* __restrict__ x, int64_t nv,
                                                         uint4* __restrict__ out) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < nv;
-       i += static_cast<int64_t>(gridDim.x) * 256) {
-    const uint4 v = ld_nc_v4(x + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * 1024; b < nv; b += static_cast<int64_t>(gridDim.x) * 1024) {
+    uint4 v[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = e5m6_encode(bf16lo_to_f32(w[k])) | (e5m6_encode(bf16hi_to_f32(w[k])) << 16);
-    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int j = 0; j < 4; ++j) {
+      const int64_t i = b + threadIdx.x + 256 * j;
+      v[j] = i < nv ? ld_nc_v4(x + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t i = b + threadIdx.x + 256 * j;
+      if (i < nv)
+        out[i] = make_uint4(e5m6_encode2(v[j].x), e5m6_encode2(v[j].y), e5m6_encode2(v[j].z), e5m6_encode2(v[j].w));
+    }
   }
 }
 
@@ -467,7 +497,7 @@ cudaError_t launch_quant_per_channel(const DeviceInfo& dev, const void* x, int64
 cudaError_t launch_cast_e5m6(const DeviceInfo& dev, const void* x, int64_t n, void* codes, cudaStream_t stream) {
   const int64_t nv = n / 8;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
-  const int64_t blocks = (nv + 255) / 256;
+  const int64_t blocks = (nv + 1023) / 1024;
   cast_e5m6_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
       static_cast<const uint4*>(x), nv, static_cast<uint4*>(codes));
   return cudaGetLastError();
