@@ -142,6 +142,8 @@ __device__ __forceinline__ uint2 dequant4(uint32_t codes, float2 s2) {
   return make_uint2(bf16x2_rn(lo), bf16x2_rn(hi));
 }
 
+// Each CTA takes the K block blockIdx.x of a pair of N blocks (2 blockIdx.y,
+// 2 blockIdx.y + 1) and issues the loads of both before converting either.
 __global__ void __launch_bounds__(256) dequant_weight_128x128_kernel(const uint4* __restrict__ q, int64_t NB,
                                                                      int64_t KB, int64_t ldq_v,
                                                                      const float* __restrict__ sw,
@@ -149,20 +151,33 @@ __global__ void __launch_bounds__(256) dequant_weight_128x128_kernel(const uint4
   const int c = threadIdx.x & 7;
   const int r0 = threadIdx.x >> 3;
   const int64_t kb = blockIdx.x;
-  for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
-    const float s = __ldg(sw + nb * KB + kb);
-    const float2 s2 = make_float2(s, s);
-    const uint4* src = q + (nb * 128 + r0) * ldq_v + kb * 8 + c;
-    uint4 v[4];
+  for (int64_t nb0 = 2 * static_cast<int64_t>(blockIdx.y); nb0 < NB; nb0 += 2 * static_cast<int64_t>(gridDim.y)) {
+    const int nblk = nb0 + 1 < NB ? 2 : 1;
+    uint4 v[2][4];
+    float s[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = ld_nc_v4(src + 32 * i * ldq_v);
-    uint4* dst = y + (nb * 128 + r0) * ldy_v + kb * 16 + 2 * c;
+    for (int b = 0; b < 2; ++b) {
+      if (b < nblk) {
+        const int64_t nb = nb0 + b;
+        s[b] = __ldg(sw + nb * KB + kb);
+        const uint4* src = q + (nb * 128 + r0) * ldq_v + kb * 8 + c;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint2 a = dequant4(v[i].x, s2), b = dequant4(v[i].y, s2);
-      const uint2 d = dequant4(v[i].z, s2), e = dequant4(v[i].w, s2);
-      dst[32 * i * ldy_v] = make_uint4(a.x, a.y, b.x, b.y);
-      dst[32 * i * ldy_v + 1] = make_uint4(d.x, d.y, e.x, e.y);
+        for (int i = 0; i < 4; ++i) v[b][i] = ld_nc_v4(src + 32 * i * ldq_v);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      if (b < nblk) {
+        const float2 s2 = make_float2(s[b], s[b]);
+        uint4* dst = y + ((nb0 + b) * 128 + r0) * ldy_v + kb * 16 + 2 * c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint2 a = dequant4(v[b][i].x, s2), bb = dequant4(v[b][i].y, s2);
+          const uint2 d = dequant4(v[b][i].z, s2), e = dequant4(v[b][i].w, s2);
+          dst[32 * i * ldy_v] = make_uint4(a.x, a.y, bb.x, bb.y);
+          dst[32 * i * ldy_v + 1] = make_uint4(d.x, d.y, e.x, e.y);
+        }
+      }
     }
   }
 }
@@ -200,7 +215,8 @@ cudaError_t launch_dequant_weight_128x128(const DeviceInfo& dev, const void* q, 
                                           const float* sw, void* y, int64_t ldy, cudaStream_t stream) {
   (void)dev;
   const int64_t NB = N / 128, KB = K / 128;
-  const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(NB < kMaxGridY ? NB : kMaxGridY));
+  const int64_t pairs = (NB + 1) / 2;
+  const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(pairs < kMaxGridY ? pairs : kMaxGridY));
   dequant_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
                                                           static_cast<uint4*>(y), ldy / 8);
   return cudaGetLastError();
