@@ -130,7 +130,10 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
 
 // ---------------------------------------------------------------------------
 // 128x128 code blocks of W [N, K] -> W^T [K, N], and the block-scale matrix
-// transposed.  One CTA per block: 16-byte loads into shared memory, then
+// transposed.  One CTA per block, N blocks fastest in the grid (concurrent
+// CTAs then write adjacent 128-byte pieces of the same W^T rows, which
+// measured faster than reading adjacent pieces of the same W rows): 16-byte
+// loads into shared memory, then
 // thread t takes the input columns 4 (t % 32) .. + 3 over the 16 rows
 // 16 (t / 32) .., reading 4x4 byte squares with 32-bit loads and transposing
 // them with byte permutes; each of its 4 output rows leaves as one 16-byte run.
@@ -141,10 +144,10 @@ __global__ void __launch_bounds__(256) transpose_weight_128x128_kernel(const uin
                                                                        uint4* __restrict__ qt, int64_t ldqt_v,
                                                                        float* __restrict__ swt) {
   __shared__ __align__(16) uint8_t blk[128 * 128];
-  const int64_t kb = blockIdx.x;
   const int cg = threadIdx.x & 31;  // input columns 4 cg .. 4 cg + 3 = output rows
   const int rg = threadIdx.x >> 5;  // input rows 16 rg .. 16 rg + 15 = output columns
-  for (int64_t nb = blockIdx.y; nb < NB; nb += gridDim.y) {
+  const int64_t nb = blockIdx.x;
+  for (int64_t kb = blockIdx.y; kb < KB; kb += gridDim.y) {
     uint4 v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -206,7 +209,7 @@ cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q
                                             cudaStream_t stream) {
   (void)dev;
   const int64_t NB = N / 128, KB = K / 128;
-  const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(NB < kMaxGridY ? NB : kMaxGridY));
+  const dim3 grid(static_cast<unsigned>(NB), static_cast<unsigned>(KB < kMaxGridY ? KB : kMaxGridY));
   transpose_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
                                                             static_cast<uint4*>(qt), ldqt / 16, swt);
   return cudaGetLastError();
