@@ -680,8 +680,8 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
 constexpr int kMinSplitChunks = 4;
 
 // Persistent launch: one cluster of CG CTAs per CG SMs, at most one per work
-// item.  When the dense tiles leave a last round that fills at most half of the
-// resident clusters, those tail tiles are split along K over the idle
+// item.  When the dense tiles leave a last round (or a single round) that fills
+// at most half of the resident clusters, those tiles are split along K over the idle
 // clusters (FP32 partials in a workspace: `scratch` when given, else
 // stream-ordered memory from the library's per-device pool) and summed by
 // split_tail_reduce_kernel.
@@ -721,8 +721,10 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   p.ws = nullptr;
   bool owned = false;
   if constexpr (!GROUPED) {
+    // the last round's tiles (all of them when the grid fills at most half of
+    // the resident clusters, e.g. skinny products with few column tiles)
     const int64_t tail = cluster_tiles % resident;
-    if (cluster_tiles > resident && tail > 0 && 2 * tail <= resident) {
+    if (tail > 0 && 2 * tail <= resident) {
       int64_t split = resident / tail;
       if (split > p.KB / kMinSplitChunks) split = p.KB / kMinSplitChunks;
       const size_t bytes = static_cast<size_t>(tail * split) * CG * BM * BN * sizeof(float);
