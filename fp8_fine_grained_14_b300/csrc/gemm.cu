@@ -16,11 +16,14 @@
 //               tcgen05.commit to free the smem stage and publish the chunk
 //   warps 2..3  idle (their warpgroup gives registers to the promotion warps)
 //   warps 4..11 promotion: tcgen05.ld the chunk (one row per thread, 64
-//               columns per load), hand the TMEM buffer back as soon as the
-//               chunk is in registers, then acc += chunk * (sa[kb][m] *
-//               sw[nb][kb]) with packed FP32 FMAs (two columns per instruction);
-//               after the last chunk, BF16 (RNE) -> swizzled smem -> TMA store
-//               (dense) or row-masked coalesced stores (grouped)
+//               columns per load), acc += chunk * (sa[kb][m] * sw[nb][kb])
+//               with packed FP32 FMAs (two columns per instruction), handing
+//               the TMEM buffer back as soon as the whole chunk has been read
+//               (for 128 columns per warp the FMAs of the first 64 run between
+//               the two loads: accumulators and 128 loaded columns do not fit
+//               in registers together); after the last chunk, BF16 (RNE) ->
+//               swizzled smem -> TMA store (dense) or row-masked coalesced
+//               stores (grouped)
 //
 // Wide tiles run on CTA pairs (CG = 2, a cluster of two CTAs on two SMs):
 // the pair computes a 256 x 256 tile with tcgen05 cta_group::2 MMAs issued by
@@ -31,9 +34,12 @@
 // and each CTA promotes and stores its own rows.  Narrow tiles (BN = 128, for
 // skinny M) run on single CTAs (CG = 1).
 //
-// The kernel is persistent: cluster c handles tiles c, c + clusters, ...;
-// tiles are ordered M-fastest so a wave shares a few weight column blocks
-// (L2-resident) and the whole activation matrix.
+// The kernel is persistent: cluster c handles work items c, c + clusters, ...;
+// dense tiles are ordered M-fastest when A is the smaller operand (a wave then
+// shares a few weight column blocks and the whole, L2-resident, activation
+// matrix) and N-fastest otherwise.  When the last round of dense tiles, or
+// the only one, would fill at most half of the clusters, those tiles are cut
+// into K slices whose FP32 partials a second kernel sums (split-K tail).
 //
 // Every mbarrier wait is bounded (see ptx.cuh).  A wait that gives up records
 // a timeout in the status word and raises a CTA-wide abort flag; every role
