@@ -57,7 +57,8 @@ __global__ void __launch_bounds__(256) quant_per_token_kernel(const uint4* __res
 }
 
 // ---------------------------------------------------------------------------
-// Per channel: (1) column maxima of |x| as BF16 bit patterns (non-negative
+// Per channel, two passes (inputs taller than the one-pass cluster kernel
+// below takes): (1) column maxima of |x| as BF16 bit patterns (non-negative
 // values order like their patterns), reduced across a CTA in shared memory
 // and merged into s with atomicMax, (2) every element quantised with its
 // column's scale, (3) s turned from maxima into scales.  A CTA covers 256
