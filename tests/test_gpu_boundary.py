@@ -75,3 +75,53 @@ def test_gemm_repeatable():
     y2 = fb.fp8_blockscaled_gemm(qa, sa, qw, sw)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+
+
+def test_empty_inputs_every_entry_point():
+    """Zero rows (or zero elements) is a no-op for every entry point, and an
+    expert group with no rows contributes nothing."""
+    z = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
+    q, s = fb.fp8_quant_per_token(z)
+    assert q.shape == (0, 256) and s.shape == (0,)
+    q, s = fb.fp8_quant_per_channel(z)
+    assert q.shape == (0, 256)
+    qa, sa, h = fb.fp8_swiglu_quant_act_1x128(torch.empty((0, 512), dtype=torch.bfloat16, device=DEV), return_h=True)
+    assert qa.shape == (0, 256) and h.shape == (0, 256)
+    assert fb.e5m6_encode(torch.empty((0,), dtype=torch.bfloat16, device=DEV)).numel() == 0
+    assert fb.e5m6_decode(torch.empty((0,), dtype=torch.int16, device=DEV)).numel() == 0
+    qt, st = fb.fp8_quant_act_1x128_t(torch.empty((0, 256), dtype=torch.bfloat16, device=DEV))
+    assert qt.shape == (256, 0)
+    qa0, sa0 = fb.fp8_quant_act_1x128(z)
+    qb, sb = fb.fp8_quant_act_1x128(torch.zeros((128, 256), dtype=torch.bfloat16, device=DEV))
+    assert fb.fp8_blockscaled_gemm_rowscaled(qa0, sa0, qb, sb).shape == (0, 128)
+    qw, sw = fb.fp8_quant_weight_128x128(torch.zeros((128, 256), dtype=torch.bfloat16, device=DEV))
+    assert fb.fp8_blockscaled_gemm_noalloc(qa0, sa0, qw, sw).shape == (0, 128)
+    # grouped: every group empty, and one empty group between two others
+    off0 = torch.zeros((3,), dtype=torch.int32, device=DEV)
+    qw3 = torch.zeros((2, 128, 256), dtype=torch.uint8, device=DEV)
+    sw3 = torch.ones((2, 1, 2), dtype=torch.float32, device=DEV)
+    assert fb.fp8_blockscaled_grouped_gemm(off0, 0, qa0, sa0, qw3, sw3).shape == (0, 128)
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+
+
+def test_grouped_empty_middle_group():
+    """Three experts, the middle one with no rows: the other two match the
+    dense oracle on their own rows."""
+    g = torch.Generator().manual_seed(4)
+    x = torch.randn(200, 256, generator=g).to(torch.bfloat16)
+    w = (torch.randn(3, 128, 256, generator=g) * 0.02).to(torch.bfloat16)
+    offsets = torch.tensor([0, 120, 120, 200], dtype=torch.int32)
+    qa, sa = fb.fp8_quant_act_1x128(x.to(DEV))
+    qw, sw = fb.fp8_quant_weight_128x128(w.reshape(384, 256).to(DEV))
+    y = fb.fp8_blockscaled_grouped_gemm(offsets.to(DEV), 200, qa, sa, qw.reshape(3, 128, 256), sw.reshape(3, 1, 2))
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    qa_r, sa_r = oracle.quant_act_1x128(f32(x))
+    parts = []
+    for gi, (r0, r1) in enumerate([(0, 120), (120, 120), (120, 200)]):
+        if r1 == r0:
+            continue
+        qw_r, sw_r = oracle.quant_weight_128x128(f32(w[gi]))
+        parts.append(oracle.blockscaled_gemm(qa_r[r0:r1], sa_r[:, r0:r1], qw_r, sw_r))
+    assert_gemm_close(f32(y), np.concatenate(parts))
