@@ -8,6 +8,7 @@ from .fp8_oracle import (  # noqa: F401
     E5M6_MAX,
     GROUP,
     blockscaled_gemm,
+    blockscaled_gemm_residual,
     blockscaled_gemm_rowscaled,
     blockscaled_grouped_gemm,
     bf16_round,

@@ -233,6 +233,17 @@ def blockscaled_gemm(qa, sa, qw, sw):
     return y
 
 
+def blockscaled_gemm_residual(qa, sa, qw, sw, r):
+    """The block-scaled GEMM with a residual added before the output rounding:
+    Y = (sum of the promoted chunks) + R, R a BF16 [M, N] matrix given as
+    float values, in float64.  Reading: the residual stream of the block is
+    added to the linear layer's FP32 result in the epilogue, and the sum is
+    rounded once to the output format ("outputs in BF16 or FP32",
+    paragraph 4 of "The Definitive Information To Deepseek").  Returns float64
+    [M, N], unrounded."""
+    return blockscaled_gemm(qa, sa, qw, sw) + np.asarray(r, dtype=np.float64)
+
+
 def blockscaled_grouped_gemm(offsets, qa, sa, qw, sw):
     """Grouped (per-expert) block-scaled GEMM.
 

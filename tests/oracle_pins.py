@@ -704,7 +704,27 @@ def pin_swiglu(o):
     assert np.all(h0 == 0)
 
 
+def pin_gemm_residual(o):
+    """Residual epilogue: all-zero weights give back the residual exactly
+    (every weight group has s = 0 and codes 0); constant operands give the
+    closed form K (448 s_x)(448 s_w) plus the residual."""
+    rng = np.random.default_rng(43)
+    M, N, K = 6, 256, 256
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    r = o.bf16_round((rng.standard_normal((M, N)) * 3.0).astype(np.float32))
+    qa, sa = o.quant_act_1x128(x)
+    qz, sz = o.quant_weight_128x128(np.zeros((N, K), dtype=np.float32))
+    assert np.array_equal(o.blockscaled_gemm_residual(qa, sa, qz, sz, r), r.astype(np.float64))
+    xc = np.full((M, K), np.float32(2.0), dtype=np.float32)
+    wc = np.full((N, K), np.float32(-0.25), dtype=np.float32)
+    qa, sa = o.quant_act_1x128(xc)
+    qw, sw = o.quant_weight_128x128(wc)
+    want = -(K * (448.0 * float(sa[0, 0])) * (448.0 * float(sw[0, 0]))) + r.astype(np.float64)
+    assert np.array_equal(o.blockscaled_gemm_residual(qa, sa, qw, sw, r), want)
+
+
 ALL_PINS = [
+    pin_gemm_residual,
     pin_codec_format_points,
     pin_codec_roundtrip,
     pin_codec_ties,

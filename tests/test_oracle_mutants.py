@@ -108,6 +108,12 @@ MUTANTS = {
     "silu_sign_flipped": (
         "return g / (1.0 + np.exp(-g)) * u",
         "return g / (1.0 + np.exp(g)) * u"),
+    "residual_subtracted": (
+        "return blockscaled_gemm(qa, sa, qw, sw) + np.asarray(r, dtype=np.float64)",
+        "return blockscaled_gemm(qa, sa, qw, sw) - np.asarray(r, dtype=np.float64)"),
+    "residual_dropped": (
+        "return blockscaled_gemm(qa, sa, qw, sw) + np.asarray(r, dtype=np.float64)",
+        "return blockscaled_gemm(qa, sa, qw, sw)"),
     "grouped_wrong_weight_scales": (
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])",
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[0])"),
