@@ -651,6 +651,11 @@ def run_rows(args):
     yd = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     emit("a3-a5 GEMM (BF16 out)", f"down {M}x{K}x{N}",
          lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm(qad, sad, qwd, swd, y=yd)), 2 * M * N * K, "TFLOP/s")
+    rres = bf16(M, K)
+    emit("NEXT1 GEMM + BF16 residual", f"down {M}x{K}x{N}, R [{M},{K}] BF16",
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm_residual(qad, sad, qwd, swd, rres, y=yd)),
+         2 * M * N * K, "TFLOP/s")
+    del rres
     # decode
     xdec = bf16(64, K)
     qdec, sdec = fb.fp8_quant_act_1x128(xdec)

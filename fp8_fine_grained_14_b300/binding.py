@@ -32,6 +32,7 @@ EXPORTS = {
     "fp8_quant_weight_128x128": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
     "fp8_blockscaled_gemm": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_gemm_noalloc": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
+    "fp8_blockscaled_gemm_residual": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_grouped_gemm": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
     "fp8_blockscaled_gemm_f32": [_p, _i64, _p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_grouped_gemm_f32": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
@@ -159,6 +160,30 @@ def fp8_blockscaled_gemm(qa, sa, qw, sw, y=None, stream=None, out_dtype=torch.bf
     st = getattr(lib, fn)(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
                           _ptr(y), y.stride(0), M, N, K, _stream(stream))
     _check(fn, st)
+    return y
+
+
+def fp8_blockscaled_gemm_residual(qa, sa, qw, sw, residual, y=None, stream=None):
+    """Y = bf16(FP32 block-scaled GEMM + residual), the residual (BF16 [M, N])
+    added before the single output rounding.  y may be `residual` itself for
+    an in-place update."""
+    _require(qa, torch.uint8, "qa", 2)
+    _require(qw, torch.uint8, "qw", 2)
+    _require(sa, torch.float32, "sa", 2)
+    _require(residual, torch.bfloat16, "residual", 2)
+    M, K = qa.shape
+    N = qw.shape[0]
+    if tuple(residual.shape) != (M, N):
+        raise ValueError("residual must be [M, N]")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    _require(y, torch.bfloat16, "y", 2)
+    if not sw.is_contiguous():
+        raise ValueError("sw must be contiguous")
+    st = lib.fp8_blockscaled_gemm_residual(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0),
+                                           _ptr(sw), _ptr(residual), residual.stride(0), _ptr(y), y.stride(0),
+                                           M, N, K, _stream(stream))
+    _check("fp8_blockscaled_gemm_residual", st)
     return y
 
 

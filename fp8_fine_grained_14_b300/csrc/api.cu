@@ -216,7 +216,8 @@ namespace {
 // 4 (FP32 y) and sets the row-stride rule for y.
 fp8bs_status dense_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw, int64_t ldqw,
                         const float* sw, void* y, int64_t ldy, int out_bytes, int64_t M, int64_t N, int64_t K,
-                        cudaStream_t stream, const char* name, bool use_static_scratch = false) {
+                        cudaStream_t stream, const char* name, bool use_static_scratch = false,
+                        const void* res = nullptr, int64_t ldr = 0) {
   if (M < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldqw < 0 || ldy < 0) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim)
     return FP8BS_ERR_UNSUPPORTED_SHAPE;
@@ -239,7 +240,7 @@ fp8bs_status dense_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t l
     scratch_bytes = fp8bs::kGemmScratchBytes;
   }
   e = fp8bs::launch_blockscaled_gemm(*dev, qa, ldqa, sa, ld_sa, qw, ldqw, sw, y, ldy, out_bytes == 4, M, N, K,
-                                     stream, scratch, scratch_bytes);
+                                     stream, scratch, scratch_bytes, res, ldr);
   if (e == cudaErrorMemoryAllocation && use_static_scratch) {
     std::snprintf(fp8bs::t_detail, sizeof(fp8bs::t_detail), "%s: split-K workspace larger than the static scratch", name);
     return FP8BS_ERR_UNSUPPORTED_SHAPE;
@@ -426,6 +427,20 @@ fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa,
                                   int64_t ldqw, const float* sw, void* y_bf16, int64_t ldy, int64_t M, int64_t N,
                                   int64_t K, cudaStream_t stream) {
   return dense_gemm(qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, 2, M, N, K, stream, "fp8_blockscaled_gemm launch");
+}
+
+fp8bs_status fp8_blockscaled_gemm_residual(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                           const void* qw, int64_t ldqw, const float* sw, const void* r_bf16,
+                                           int64_t ldr, void* y_bf16, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                                           cudaStream_t stream) {
+  if (ldr < 0) return FP8BS_ERR_INVALID_ARG;
+  if (M > 0) {
+    if (r_bf16 == nullptr || ldr < N) return FP8BS_ERR_INVALID_ARG;
+    if (r_bf16 == y_bf16 && ldr != ldy) return FP8BS_ERR_INVALID_ARG;  // in place: same layout
+    if (!aligned16(r_bf16) || ldr % 8 != 0) return FP8BS_ERR_MISALIGNED;
+  }
+  return dense_gemm(qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, 2, M, N, K, stream,
+                    "fp8_blockscaled_gemm_residual launch", false, r_bf16, ldr);
 }
 
 fp8bs_status fp8_blockscaled_gemm_noalloc(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,

@@ -64,6 +64,7 @@ constexpr int kEpiWarps = 8;          // warps 4..11
 constexpr int kFirstEpiWarp = 4;
 constexpr int kStagingBytes = 4096;   // per promotion warp: 32 rows x 64 BF16
 constexpr int kEpiRowBytes = 128;     // bytes of one staged output row (one 128B-swizzle row)
+constexpr int kResPrefetchChunks = 4;  // residual epilogue: L2 prefetch this many chunks before the end
 // Register split for 256-wide tiles (setmaxnreg): warpgroup 0 (TMA, MMA,
 // idle) drops to RegSplit::low, the two promotion warpgroups rise to
 // RegSplit::high.  Every SM sub-partition hosts one warp of each warpgroup, so
@@ -103,7 +104,16 @@ struct Params {
   int32_t t_full;
   int32_t split;
   float* ws;
+  // Dense only: BF16 residual R [M, N] (row stride ldr) added to the FP32
+  // result before the output rounding; null when there is none.
+  const uint16_t* res;
+  int64_t ldr;
 };
+
+// Adds 2 or 4 BF16 residual values (one 32-bit word each pair) to FP32 pairs.
+__device__ __forceinline__ float2 add_bf16_pair(float2 a, uint32_t r) {
+  return make_float2(__fadd_rn(a.x, bf16lo_to_f32(r)), __fadd_rn(a.y, bf16hi_to_f32(r)));
+}
 
 // Origin of dense cluster tile `tile` (see TileWalker for the order).
 template <int BN, int CM>
@@ -232,13 +242,14 @@ __device__ __forceinline__ void abort_cta(volatile int* abort_flag, unsigned* st
   record_status(status, kStatusTimeout);
 }
 
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false, bool RES = false>
 __global__ void __launch_bounds__(kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmY, const Params p) {
   using L = Smem<BN, STAGES, CG, RS, HALF_A>;
   static_assert(!HALF_A || (CG == 1 && !GROUPED), "64-row A tiles are a dense single-CTA variant");
   static_assert(!(RS && GROUPED), "row-scaled B is a dense-only variant");
+  static_assert(!RES || (!GROUPED && !RS && !F32), "the residual epilogue is a dense BF16-output variant");
   static_assert(CG == 1 || CG == 2, "single CTAs or CTA pairs");
   constexpr int kTmemCols = 2 * BN;   // two accumulator buffers of this CTA's 128 rows x BN
   constexpr int kHalfCols = BN / 2;   // columns per promotion warp
@@ -462,6 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         sa_next = __ldg(sa_col + static_cast<int64_t>(kn) * p.ld_sa);
         if (!RS) sw_next = __ldg(sw_row + kn);
         const float* cs = colscale + ((kb - kb0) & 1) * kHalfCols;  // this chunk's column scales (RS)
+        if (RES && row_ok && kb == (kb1 - kb0 > kResPrefetchChunks ? kb1 - kResPrefetchChunks : kb0)) {
+          // a few chunks before the epilogue: pull this row's residual
+          // segment into L2 so that the epilogue's loads do not wait on DRAM
+          const uint16_t* rp = p.res + static_cast<int64_t>(row) * p.ldr + col0;
+#pragma unroll
+          for (int l = 0; l < kHalfCols / 64; ++l) prefetch_l2(rp + 64 * l);
+        }
         const bool waited = mbar_wait(bar_tfull + 8 * buf, bphase, abort_flag, p.timeout_ns);
         if (!__all_sync(0xffffffffu, waited)) {
           abort_cta(abort_flag, p.status);
@@ -554,6 +572,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8; ++j) {
           // 16 bytes: 8 BF16 or 4 FP32 outputs of this thread's row
           const int c0 = (piece * kPieceCols + j * (16 / kOutBytes)) / 2;
+          if (RES && row_ok) {
+            // residual epilogue: R added to the FP32 result, one rounding after
+            const uint16_t* rp =
+                p.res + static_cast<int64_t>(row) * p.ldr + col0 + piece * kPieceCols + j * (16 / kOutBytes);
+            if (F32) {
+              const uint2 rr = *reinterpret_cast<const uint2*>(rp);
+              acc[c0] = add_bf16_pair(acc[c0], rr.x);
+              acc[c0 + 1] = add_bf16_pair(acc[c0 + 1], rr.y);
+            } else {
+              const uint4 rr = *reinterpret_cast<const uint4*>(rp);
+              acc[c0] = add_bf16_pair(acc[c0], rr.x);
+              acc[c0 + 1] = add_bf16_pair(acc[c0 + 1], rr.y);
+              acc[c0 + 2] = add_bf16_pair(acc[c0 + 2], rr.z);
+              acc[c0 + 3] = add_bf16_pair(acc[c0 + 3], rr.w);
+            }
+          }
           uint4 v;
           if (F32) {
             v = make_uint4(__float_as_uint(acc[c0].x), __float_as_uint(acc[c0].y), __float_as_uint(acc[c0 + 1].x),
@@ -646,6 +680,12 @@ __global__ void __launch_bounds__(256) split_tail_reduce_kernel(const Params p) 
       sum.w = __fadd_rn(sum.w, v.w);
     }
     if (row < p.M) {
+      if (p.res != nullptr) {
+        const uint2 rr = *reinterpret_cast<const uint2*>(p.res + static_cast<int64_t>(row) * p.ldr + col0 + 4 * j);
+        const float2 lo = add_bf16_pair(make_float2(sum.x, sum.y), rr.x);
+        const float2 hi = add_bf16_pair(make_float2(sum.z, sum.w), rr.y);
+        sum = make_float4(lo.x, lo.y, hi.x, hi.y);
+      }
       const int64_t off = static_cast<int64_t>(row) * p.ldy + col0 + 4 * j;
       if (F32) {
         *reinterpret_cast<float4*>(static_cast<float*>(p.y) + off) = sum;
@@ -661,7 +701,7 @@ __global__ void __launch_bounds__(256) split_tail_reduce_kernel(const Params p) 
 
 // Largest number of clusters of this kernel variant that can be resident at
 // once on the current device (queried once per device and variant).
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A, bool RES>
 int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) {
   static std::atomic<int> cache[64];
   const int idx = dev.ordinal & 63;
@@ -670,7 +710,7 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
   n = dev.num_sms / CG;
   if (CG > 1) {
     int q = 0;
-    if (cudaOccupancyMaxActiveClusters(&q, blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>, &cfg) == cudaSuccess &&
+    if (cudaOccupancyMaxActiveClusters(&q, blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A, RES>, &cfg) == cudaSuccess &&
         q > 0)
       n = q;
     else
@@ -691,12 +731,12 @@ constexpr int kMinSplitChunks = 4;
 // clusters (FP32 partials in a workspace: `scratch` when given, else
 // stream-ordered memory from the library's per-device pool) and summed by
 // split_tail_reduce_kernel.
-template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false>
+template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false, bool RES = false>
 cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                           const CUtensorMap& tmY, const Params& p0, int64_t cluster_tiles, cudaStream_t stream,
                           float* scratch, size_t scratch_bytes) {
   using L = Smem<BN, STAGES, CG, RS, HALF_A>;
-  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>;
+  auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A, RES>;
   if (BN == 256) {
     // setmaxnreg.inc only completes if the launch holds kRegsLaunch registers
     // per thread; refuse to launch a build that does not.
@@ -719,7 +759,7 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(CG, 1, 1);
-  const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32, RS, HALF_A>(dev, cfg);
+  const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32, RS, HALF_A, RES>(dev, cfg);
   Params p = p0;
   p.n_items = static_cast<int32_t>(cluster_tiles);
   p.t_full = static_cast<int32_t>(cluster_tiles);
@@ -798,6 +838,8 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
   p.sw = sw;
   p.sb = nullptr;
   p.ld_sb = 0;
+  p.res = nullptr;
+  p.ldr = 0;
   p.y = y;
   p.ldy = ldy;
   p.M = static_cast<int32_t>(M);
@@ -816,24 +858,24 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
 // pair (BN = 256 on a CTA pair, 256 x 256 per pair).
 enum class Shape { kNarrow, kNarrowHalfA, kWide, kPair };
 
-template <bool GROUPED, bool F32, bool RS = false>
+template <bool GROUPED, bool F32, bool RS = false, bool RES = false>
 cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream,
                          float* scratch = nullptr, size_t scratch_bytes = 0) {
   switch (shape) {
     case Shape::kNarrow:
-      return launch_kernel<128, RS ? kStages128RS : kStages128, GROUPED, 1, F32, RS>(
+      return launch_kernel<128, RS ? kStages128RS : kStages128, GROUPED, 1, F32, RS, false, RES>(
           dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
     case Shape::kNarrowHalfA:
       if constexpr (!GROUPED && !RS)
-        return launch_kernel<128, kStages128HalfA, false, 1, F32, false, true>(dev, tmA, tmB, tmY, p, cluster_tiles,
+        return launch_kernel<128, kStages128HalfA, false, 1, F32, false, true, RES>(dev, tmA, tmB, tmY, p, cluster_tiles,
                                                                              stream, scratch, scratch_bytes);
       return cudaErrorInvalidValue;
     case Shape::kWide:
-      return launch_kernel<256, RS ? kStages256RS : kStages256, GROUPED, 1, F32, RS>(
+      return launch_kernel<256, RS ? kStages256RS : kStages256, GROUPED, 1, F32, RS, false, RES>(
           dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
     case Shape::kPair:
-      return launch_kernel<256, RS ? kStagesPairRS : kStagesPair, GROUPED, 2, F32, RS>(
+      return launch_kernel<256, RS ? kStagesPairRS : kStagesPair, GROUPED, 2, F32, RS, false, RES>(
           dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
   }
   return cudaErrorInvalidValue;
@@ -844,7 +886,7 @@ cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& 
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
                                     int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                                    float* scratch, size_t scratch_bytes) {
+                                    float* scratch, size_t scratch_bytes, const void* res, int64_t ldr) {
   // Wide tiles (BN = 256) halve the operand traffic per FLOP; narrow ones keep
   // every SM busy when there are few tiles (skinny, decode-shaped M).
   const int64_t m_tiles = (M + BM - 1) / BM;
@@ -861,8 +903,17 @@ cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64
       !make_tmap_2d(&tmY, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M,
                     ldy * out_bytes, kEpiRowBytes / out_bytes, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const Params p = make_params(dev, sa, ld_sa, sw, y, ldy, M, N, K, nullptr, 1);
+  Params p = make_params(dev, sa, ld_sa, sw, y, ldy, M, N, K, nullptr, 1);
+  p.res = static_cast<const uint16_t*>(res);
+  p.ldr = ldr;
   const int64_t cluster_tiles = (m_tiles + CG - 1) / CG * (N / BN);
+  if (res != nullptr) {
+    // the residual epilogue is its own kernel variant (BF16 output only), so
+    // the plain GEMM keeps its register budget
+    if (y_f32) return cudaErrorInvalidValue;
+    return launch_shape<false, false, false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch,
+                                                   scratch_bytes);
+  }
   return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes)
                : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch,
                                             scratch_bytes);

@@ -40,11 +40,14 @@ cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, in
 // When the last round of tiles would leave most SMs idle, the tail tiles are
 // split along K; their FP32 partials go to `scratch` (scratch_bytes long; the
 // launch fails with cudaErrorMemoryAllocation if it is too small) or, when scratch
-// is null, to stream-ordered memory from DeviceInfo::workspace_pool.
+// is null, to stream-ordered memory from DeviceInfo::workspace_pool.  res (BF16,
+// row stride ldr elements), when not null, is added to the FP32 result before
+// the output rounding; it may be y itself (same stride) for an in-place update.
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
                                     int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                                    float* scratch = nullptr, size_t scratch_bytes = 0);
+                                    float* scratch = nullptr, size_t scratch_bytes = 0, const void* res = nullptr,
+                                    int64_t ldr = 0);
 
 cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,
                                             int64_t M_total, const void* qa, int64_t ldqa, const float* sa,

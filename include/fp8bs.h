@@ -256,6 +256,21 @@ fp8bs_status fp8_swiglu_quant_act_1x128(const void* gate_up_bf16, int64_t M, int
                                         void* h_bf16, int64_t ldh, cudaStream_t stream);
 
 /*
+ * fp8_blockscaled_gemm with a residual: Y = bf16_rn(fl32(sum) + R), where the
+ * FP32 result of the block-scaled GEMM and the BF16 residual R [M, N] (row
+ * stride ldr elements) are added before the single rounding to BF16
+ * ("The Definitive Information To Deepseek", paragraph 4: BF16 or FP32
+ * outputs; the addition fuses the block's residual stream into the
+ * epilogue).  R and Y are either the same buffer with the same stride (an
+ * in-place update of the residual stream) or disjoint.  R must be 16-byte
+ * aligned with ldr % 8 == 0 and ldr >= N; otherwise as fp8_blockscaled_gemm.
+ */
+fp8bs_status fp8_blockscaled_gemm_residual(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                           const void* qw, int64_t ldqw, const float* sw,
+                                           const void* r_bf16, int64_t ldr, void* y_bf16, int64_t ldy,
+                                           int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * fp8_blockscaled_gemm without any allocation.  The pages have no counterpart
  * of this call: it exists for callers that must not allocate (e.g. inside
  * graph capture with allocation disabled).  Same arguments, layouts, results

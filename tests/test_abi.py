@@ -117,3 +117,16 @@ def test_dequant_validation(lib, args, expect):
 ])
 def test_grouped_validation(lib, args, expect):
     assert lib.fp8_blockscaled_grouped_gemm(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 128, A16, 4, A16, 128, A16, None, 128, A16, 128, 1, 128, 128, None), 1),        # null residual
+    ((A16, 128, A16, 4, A16, 128, A16, A16, 120, A16, 128, 1, 128, 128, None), 1),         # ldr < N
+    ((A16, 128, A16, 4, A16, 128, A16, A16, 128, A16, 136, 1, 128, 128, None), 1),         # in place, ldr != ldy
+    ((A16, 128, A16, 4, A16, 128, A16, P(0x10002), 128, A16, 128, 1, 128, 128, None), 2),  # misaligned residual
+    ((A16, 128, A16, 4, A16, 128, A16, P(0x20000), 132, A16, 128, 1, 128, 128, None), 2),  # ldr % 8
+    ((A16, 128, A16, 4, A16, 128, A16, P(0x20000), 128, A16, 128, 1, 100, 128, None), 3),  # N % 128
+    ((A16, 128, A16, 4, A16, 128, A16, None, 0, A16, 128, 0, 128, 128, None), 0),          # M == 0
+])
+def test_gemm_residual_validation(lib, args, expect):
+    assert lib.fp8_blockscaled_gemm_residual(*args) == expect
