@@ -110,7 +110,14 @@ struct Params {
   int64_t ldr;
 };
 
-// Adds 2 or 4 BF16 residual values (one 32-bit word each pair) to FP32 pairs.
+// Bring the 128-byte line holding `ptr` into L2 (a hint; no fault on any
+// address the caller may also load).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
+}
+
+// Adds a pair of BF16 residual values (one 32-bit word) to a pair of FP32
+// accumulators, each sum rounded to FP32.
 __device__ __forceinline__ float2 add_bf16_pair(float2 a, uint32_t r) {
   return make_float2(__fadd_rn(a.x, bf16lo_to_f32(r)), __fadd_rn(a.y, bf16hi_to_f32(r)));
 }

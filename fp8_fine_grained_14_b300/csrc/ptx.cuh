@@ -111,12 +111,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 // ---------------------------------------------------------------------------
 // TMA (tensor-map bulk copies)
 // ---------------------------------------------------------------------------
-// Bring the 128-byte line holding `ptr` into L2 (a hint; no fault on any
-// address the caller may also load).
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
-}
-
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
