@@ -12,6 +12,7 @@ from .fp8_oracle import (  # noqa: F401
     blockscaled_gemm_rowscaled,
     blockscaled_grouped_gemm,
     bf16_round,
+    dequant_act_1x128_bf16,
     dequant_weight_128x128,
     dequant_weight_128x128_bf16,
     e4m3_decode,
@@ -20,6 +21,7 @@ from .fp8_oracle import (  # noqa: F401
     e5m6_encode_rne_satfinite,
     fl32_div,
     linear_backward,
+    linear_backward_cached,
     linear_forward,
     quant_act_1x128,
     quant_act_1x128_t,
@@ -28,5 +30,6 @@ from .fp8_oracle import (  # noqa: F401
     silu_mul,
     swiglu_quant_act_1x128,
     quant_weight_128x128,
+    requant_act_1x128_t,
     transpose_weight_128x128,
 )

@@ -407,14 +407,53 @@ def linear_backward(x, w, dy):
     """Both backward GEMMs on float32 inputs holding BF16 values:
     dX = Q(dY) . Q(W)^T-blocks and dW = Q(dY^T) . Q(X^T)^T.
     Returns (dx float64 [M, K], dw float64 [N, K])."""
+    return _linear_backward_from(quant_act_1x128_t(x), w, dy)
+
+
+def _linear_backward_from(xt, w, dy):
+    """The two backward GEMMs given X's weight-gradient operand xt = (codes
+    [K, M], scales [M/128, K])."""
     qw, sw = quant_weight_128x128(w)
     qdy, sdy = quant_act_1x128(dy)
     qwt, swt = transpose_weight_128x128(qw, sw)
     dx = blockscaled_gemm(qdy, sdy, qwt, swt)
     qdyt, sdyt = quant_act_1x128_t(dy)
-    qxt, sxt = quant_act_1x128_t(x)
+    qxt, sxt = xt
     dw = blockscaled_gemm_rowscaled(qdyt, sdyt, qxt, sxt)
     return dx, dw
+
+
+def dequant_act_1x128_bf16(qa, sa):
+    """BF16 activation back from its cached 1x128 FP8 form: for each element,
+    bf16(fl32(dec(qa[m, k]) * sa[k // 128, m])), the same float32 product
+    and single BF16 rounding as dequant_weight_128x128_bf16 with the 1x128
+    grouping.  qa uint8 [M, K], sa float32 [K/128, >=M].  Returns float32
+    [M, K] holding BF16 values."""
+    qa = np.asarray(qa, dtype=np.uint8)
+    M, K = qa.shape
+    sa = np.asarray(sa, dtype=np.float32)[:, :M]
+    scale = np.repeat(np.ascontiguousarray(sa.T), GROUP, axis=1)   # [M, K]: row m, chunk k // 128
+    prod = e4m3_decode(qa).astype(np.float32) * scale              # float32 multiply, rounded once
+    x = bf16_round(prod)
+    return x
+
+
+def requant_act_1x128_t(qa, sa):
+    """The weight-gradient operand from the activation cached in FP8 for the
+    backward pass (paragraph 2 of "The Definitive Information To Deepseek"):
+    the cached 1x128 codes are dequantised to BF16 (above), and that matrix
+    is quantised on 1x128 tiles of its transpose (per channel per 128
+    tokens), exactly as quant_act_1x128_t does for a BF16 activation.
+    Returns codes [K, M] and scales [M/128, K].  M % 128 == 0."""
+    return quant_act_1x128_t(dequant_act_1x128_bf16(qa, sa))
+
+
+def linear_backward_cached(qa, sa, w, dy):
+    """linear_backward with the activation taken from its cached FP8 form
+    (qa, sa) -- the forward's 1x128 quantisation of X -- instead of BF16 X:
+    dW = Q(dY^T) . R(qa, sa)^T with R = requant_act_1x128_t; dX as in
+    linear_backward.  Returns (dx float64 [M, K], dw float64 [N, K])."""
+    return _linear_backward_from(requant_act_1x128_t(qa, sa), w, dy)
 
 
 def linear_forward(x, w):

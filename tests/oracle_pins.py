@@ -723,7 +723,89 @@ def pin_gemm_residual(o):
     assert np.array_equal(o.blockscaled_gemm_residual(qa, sa, qw, sw, r), want)
 
 
+def pin_act_dequant(o):
+    """dequant of the cached 1x128 activation: quant then dequant stays within
+    half an E4M3 ulp of each group (times its scale) plus the BF16 rounding;
+    with scales constant over 128x128 blocks it equals the weight dequant
+    (which indexes its scales the other way round); the float32 product is
+    rounded to BF16 once more (0x39 = 1.125 times 1.0078125 -> 1.1328125)."""
+    rng = np.random.default_rng(71)
+    x = (rng.standard_normal((256, 384)) * np.exp(rng.standard_normal((256, 1)) * 3)).astype(np.float32)
+    x[5, 128:256] = 0.0
+    qa, sa = o.quant_act_1x128(x)
+    y = o.dequant_act_1x128_bf16(qa, sa).astype(np.float64)
+    s = np.repeat(sa.T.astype(np.float64), 128, axis=1)
+    v = np.abs(x.astype(np.float64)) / np.where(s > 0, s, 1)
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -6)))
+    ulp = np.where(v < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
+    bound = 0.5 * ulp * s * (1 + 2.0 ** -20) + np.abs(x) * 2.0 ** -8 + 1e-300
+    assert np.all(np.abs(y - x) <= bound)
+    assert np.all(y[5, 128:256] == 0.0)
+    q = rng.integers(0, 256, (256, 384)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x11  # no NaN codes
+    sw = rng.uniform(0.5, 2.0, (2, 3)).astype(np.float32)
+    sa_blocks = np.repeat(sw.T, 128, axis=1)  # sa[kb, m] = sw[m // 128, kb]
+    assert np.array_equal(o.dequant_act_1x128_bf16(q, sa_blocks).view(np.uint32),
+                          o.dequant_weight_128x128_bf16(q, sw).view(np.uint32))
+    q1 = np.full((3, 128), 0x39, dtype=np.uint8)
+    got = o.dequant_act_1x128_bf16(q1, np.full((1, 4), 1.0078125, dtype=np.float32))
+    assert got.shape == (3, 128) and np.all(got == np.float32(1.1328125))
+
+
+def pin_requant_transpose_identity(o):
+    """When every scale is a power of two, constant over each 128x128 tile,
+    and each column of each tile holds a +-448 code, the dequantised values
+    are exact and every (128-token, channel) group has amax 448 s: the
+    requantised codes of X^T are the cached codes transposed, bit for bit,
+    and its scales are the tile scales in the [M/128, K] layout."""
+    rng = np.random.default_rng(73)
+    M, K = 256, 384
+    q = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x22
+    q[rng.integers(0, 128, K), np.arange(K)] = 0x7E            # a +448 code in every column of tile row 0
+    q[128 + rng.integers(0, 128, K), np.arange(K)] = 0xFE      # a -448 code in every column of tile row 1
+    e = rng.integers(-12, 12, (K // 128, M // 128))            # exponent of tile (kb, mb)
+    sa = np.repeat(np.ldexp(1.0, e), 128, axis=1).astype(np.float32)  # [K/128, M]
+    qt, st = o.requant_act_1x128_t(q, sa)
+    assert qt.shape == (K, M) and st.shape == (M // 128, K)
+    assert np.array_equal(qt, q.T)
+    assert np.array_equal(st, np.repeat(np.ldexp(1.0, e.T), 128, axis=1).astype(np.float32))
+
+
+def pin_backward_cached(o):
+    """With X exactly representable by its 1x128 quantisation (each group a
+    power of two times E4M3 values, one of them +-448), the cached-activation
+    backward equals the BF16-activation backward exactly; on general X its dW
+    stays within the E4M3 worst case of the unquantised product."""
+    rng = np.random.default_rng(79)
+    M, N, K = 256, 128, 256
+    codes = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x30
+    codes[np.arange(M), rng.integers(0, 128, M)] = 0x7E
+    codes[np.arange(M), 128 + rng.integers(0, 128, M)] = 0xFE
+    e = rng.integers(-6, 6, (M, K // 128))
+    x = (o.e4m3_decode(codes) * np.repeat(np.ldexp(1.0, e), 128, axis=1)).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    dy = rng.standard_normal((M, N)).astype(np.float32)
+    qa, sa = o.quant_act_1x128(x)
+    assert np.array_equal(qa, codes)
+    dx_c, dw_c = o.linear_backward_cached(qa, sa, w, dy)
+    dx, dw = o.linear_backward(x, w, dy)
+    assert np.array_equal(dx_c, dx) and np.array_equal(dw_c, dw)
+    xg = rng.standard_normal((M, K)).astype(np.float32)
+    qg, sg = o.quant_act_1x128(xg)
+    _, dw_g = o.linear_backward_cached(qg, sg, w, dy)
+    exact = dy.astype(np.float64).T @ xg.astype(np.float64)
+    # X goes through two E4M3 roundings (1x128, then 128 tokens), dY through one
+    mag = np.abs(dy.astype(np.float64)).T @ np.abs(xg.astype(np.float64))
+    rel = (1 + 2.0 ** -4) ** 2 * (1 + 2.0 ** -8) * (1 + 2.0 ** -4) - 1
+    assert np.all(np.abs(dw_g - exact) <= rel * mag + 2.0 ** -6)
+
+
 ALL_PINS = [
+    pin_act_dequant,
+    pin_requant_transpose_identity,
+    pin_backward_cached,
     pin_gemm_residual,
     pin_codec_format_points,
     pin_codec_roundtrip,

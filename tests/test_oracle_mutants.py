@@ -114,6 +114,18 @@ MUTANTS = {
     "residual_dropped": (
         "return blockscaled_gemm(qa, sa, qw, sw) + np.asarray(r, dtype=np.float64)",
         "return blockscaled_gemm(qa, sa, qw, sw)"),
+    "act_dequant_scale_rows_reversed": (
+        "scale = np.repeat(np.ascontiguousarray(sa.T), GROUP, axis=1)",
+        "scale = np.repeat(np.ascontiguousarray(sa.T[::-1]), GROUP, axis=1)"),
+    "act_dequant_not_rounded_to_bf16": (
+        "x = bf16_round(prod)",
+        "x = prod"),
+    "requant_not_transposed": (
+        "return quant_act_1x128_t(dequant_act_1x128_bf16(qa, sa))",
+        "return quant_act_1x128(dequant_act_1x128_bf16(qa, sa))"),
+    "cached_backward_requantises_dy": (
+        "return _linear_backward_from(requant_act_1x128_t(qa, sa), w, dy)",
+        "return _linear_backward_from(quant_act_1x128_t(dy), w, dy)"),
     "grouped_wrong_weight_scales": (
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[g])",
         "y[r0:r1] = blockscaled_gemm(qa[r0:r1], sa[:, r0:r1], qw[g], sw[0])"),
