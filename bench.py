@@ -78,6 +78,13 @@ WORKLOAD_TEXT = {
 # Algorithmic work per kernel launch (each operand read once, each output
 # written once; re-reads caused by tiling are not counted).
 # ---------------------------------------------------------------------------
+def requant_bytes(M, K):
+    """FP8-cached activation -> 1x128 tiles of its transpose: the codes read
+    and written once (1 B + 1 B per element) and one FP32 scale per 128
+    elements on each side."""
+    return 2 * M * K + 8 * (M * K // 128)
+
+
 def act_quant_bytes(M, K):
     return 2 * M * K + M * K + 4 * M * (K // 128)
 
@@ -111,8 +118,8 @@ def source_digest(files):
 KERNEL_SOURCES = {
     "gemm": ["gemm.cu", "ptx.cuh"],
     "grouped_gemm": ["gemm.cu", "ptx.cuh"],
-    "act_quant": ["quant.cu", "ptx.cuh"],
-    "weight_quant": ["quant.cu", "ptx.cuh"],
+    "act_quant": ["quant.cu", "quant_common.cuh", "ptx.cuh"],
+    "weight_quant": ["quant.cu", "quant_common.cuh", "ptx.cuh"],
 }
 
 
@@ -692,6 +699,10 @@ def run_rows(args):
     emit("NEXT2 act quant of X^T", f"X [{M},{K}]",
          lambda: _time_kernel(lambda: fb.fp8_quant_act_1x128_t(x, qt=qt, st=st)), act_quant_bytes(M, K), "GB/s",
          lambda: oracle.quant_act_1x128_t(bf16c(256, 1024)), act_quant_bytes(256, 1024), "X[:256, :1024]")
+    qxs, sxs = oracle.quant_act_1x128(bf16c(256, 1024))
+    emit("NEXT2 requant of FP8-cached X^T", f"qa [{M},{K}] + 1x128 scales -> X^T codes + scales",
+         lambda: _time_kernel(lambda: fb.fp8_requant_act_1x128_t(qa, sa, qt=qt, st=st)), requant_bytes(M, K), "GB/s",
+         lambda: oracle.requant_act_1x128_t(qxs, sxs), requant_bytes(256, 1024), "qa[:256, :1024]")
     qwt = torch.empty((K, N), dtype=torch.uint8, device=dev)
     swt = torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev)
     emit("NEXT2 weight code transpose", f"W codes [{N},{K}]",

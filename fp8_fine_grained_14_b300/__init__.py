@@ -17,6 +17,7 @@ _API = (
     "fp8_blockscaled_grouped_gemm",
     "fp8_dequant_weight_128x128",
     "fp8_quant_act_1x128_t",
+    "fp8_requant_act_1x128_t",
     "fp8_transpose_weight_128x128",
     "fp8_blockscaled_gemm_rowscaled",
     "linear_backward",

@@ -38,6 +38,7 @@ EXPORTS = {
     "fp8_blockscaled_grouped_gemm_f32": [_i32, _p, _i64, _p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _p],
     "fp8_dequant_weight_128x128": [_p, _i64, _i64, _i64, _p, _p, _i64, _p],
     "fp8_quant_act_1x128_t": [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
+    "fp8_requant_act_1x128_t": [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
     "fp8_quant_per_token": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
     "fp8_quant_per_channel": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
     "fp8bs_e5m6_encode_bf16": [_p, _i64, _p, _p],
@@ -271,6 +272,26 @@ def fp8_quant_act_1x128_t(x, qt=None, st=None, stream=None):
     return qt, st
 
 
+def fp8_requant_act_1x128_t(qa, sa, qt=None, st=None, stream=None):
+    """The FP8-cached activation (qa uint8 [M, K] 1x128 codes, sa float32
+    [K/128, >=M] scales) -> (qt uint8 [K, M], st float32 [M/128, K]): each
+    value dequantised to BF16, then 1x128 tiles of the transpose, as
+    fp8_quant_act_1x128_t.  M % 128 == 0."""
+    _require(qa, torch.uint8, "qa", 2)
+    _require(sa, torch.float32, "sa", 2)
+    M, K = qa.shape
+    if qt is None:
+        qt = torch.empty((K, M), dtype=torch.uint8, device=qa.device)
+    if st is None:
+        st = torch.empty((M // 128, ld_sa_for(K)), dtype=torch.float32, device=qa.device)
+    _require(qt, torch.uint8, "qt", 2)
+    _require(st, torch.float32, "st", 2)
+    status = lib.fp8_requant_act_1x128_t(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), M, K, _ptr(qt),
+                                         qt.stride(0), _ptr(st), st.stride(0), _stream(stream))
+    _check("fp8_requant_act_1x128_t", status)
+    return qt, st
+
+
 def fp8_transpose_weight_128x128(qw, sw, qwt=None, swt=None, stream=None):
     """(qw uint8 [N, K], sw [N/128, K/128]) -> (qw^T [K, N], sw^T [K/128, N/128])."""
     _require(qw, torch.uint8, "qw", 2)
@@ -370,16 +391,21 @@ def fp8_swiglu_quant_act_1x128(gate_up, qa=None, sa=None, h=None, return_h=False
     return (qa, sa, h) if return_h else (qa, sa)
 
 
-def linear_backward(x, w, dy, stream=None, grad_dtype=torch.float32):
+def linear_backward(x, w, dy, stream=None, grad_dtype=torch.float32, x_cache=None):
     """Both backward GEMMs of the FP8 linear layer, all in the library's
     kernels: dX = Q(dY) . Q(W)^T-blocks (BF16) and dW = Q(dY^T) . Q(X^T)^T
-    (FP32 by default).  Returns (dx, dw)."""
+    (FP32 by default).  With x_cache = (qa, sa), the forward's 1x128 codes
+    and scales of X, dW takes X from that FP8 cache
+    (fp8_requant_act_1x128_t) and x may be None.  Returns (dx, dw)."""
     qw, sw = fp8_quant_weight_128x128(w, stream=stream)
     qwt, swt = fp8_transpose_weight_128x128(qw, sw, stream=stream)
     qdy, sdy = fp8_quant_act_1x128(dy, stream=stream)
     dx = fp8_blockscaled_gemm(qdy, sdy, qwt, swt, stream=stream)
     qdyt, sdyt = fp8_quant_act_1x128_t(dy, stream=stream)
-    qxt, sxt = fp8_quant_act_1x128_t(x, stream=stream)
+    if x_cache is not None:
+        qxt, sxt = fp8_requant_act_1x128_t(*x_cache, stream=stream)
+    else:
+        qxt, sxt = fp8_quant_act_1x128_t(x, stream=stream)
     dw = fp8_blockscaled_gemm_rowscaled(qdyt, sdyt, qxt, sxt, stream=stream, out_dtype=grad_dtype)
     return dx, dw
 

@@ -329,6 +329,24 @@ fp8bs_status fp8_quant_act_1x128_t(const void* x_bf16, int64_t M, int64_t K, int
   return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_act_1x128_t launch", e);
 }
 
+fp8bs_status fp8_requant_act_1x128_t(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, int64_t M,
+                                     int64_t K, void* qt, int64_t ldqt, float* st, int64_t ld_st,
+                                     cudaStream_t stream) {
+  if (M < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldqt < 0 || ld_st < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || M % 128 != 0 || K > kMaxDim || M > kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldqa < K || ld_sa < M || ldqt < M || ld_st < K) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (qa == nullptr || sa == nullptr || qt == nullptr || st == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qt) || !aligned16(st) || ldqa % 16 != 0 || ld_sa % 4 != 0 ||
+      ldqt % 16 != 0 || ld_st % 4 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_requant_act_1x128_t(*dev, qa, ldqa, sa, ld_sa, M, K, qt, ldqt, st, ld_st, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_requant_act_1x128_t launch", e);
+}
+
 fp8bs_status fp8_transpose_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, const float* sw,
                                           void* qwt, int64_t ldqt, float* swt, cudaStream_t stream) {
   if (N < 0 || K < 0 || ldq < 0 || ldqt < 0) return FP8BS_ERR_INVALID_ARG;

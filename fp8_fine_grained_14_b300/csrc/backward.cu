@@ -11,7 +11,10 @@
 //   dW = dY^T . X   reduces over tokens, so dY and X are quantised on 1x128
 //                   tiles of their transposes, i.e. per channel per 128 tokens
 //                   (quant_act_1x128_t_kernel), and multiplied by the row-scaled
-//                   GEMM (gemm.cu).
+//                   GEMM (gemm.cu).  X may also come from its FP8 cache, the
+//                   forward's 1x128 codes and scales: each value is dequantised
+//                   to BF16 (bf16_rn(fl32(dec(q) * s))) in registers and then
+//                   quantised the same way, without a BF16 copy of X in HBM.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -23,16 +26,33 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // 1x128 quantisation of X^T.  Tiles of 128 rows (tokens) x 128 columns
-// (channels) of X arrive by TMA in a 3-stage ring (persistent CTAs, two per
-// SM).  Thread t owns the column pair cp = t % 64 (channels 2cp, 2cp+1) over
-// the 32 rows 32 * (t / 64) ..; per-column maxima combine across the four row
-// quarters through shared memory; each thread then codes its 2 x 32 values and
-// writes them as two 32-byte runs of X^T's rows.  Scales go to
+// (channels) of X arrive by TMA in a ring of 96 KB (persistent CTAs, two per
+// SM): 3 stages of BF16 tiles, or 6 of FP8 code tiles when X comes from its
+// FP8 cache.  Thread t owns the column pair cp = t % 64 (channels 2cp, 2cp+1)
+// over the 32 rows 32 * (t / 64) ..; cached codes are dequantised to BF16 with
+// their rows' scales as they are read (the tile's 128 row scales travel with
+// it: a 512-byte bulk copy on the same barrier).  Per-column maxima combine across the
+// four row quarters through shared memory; each thread then codes its 2 x 32
+// values and writes them as two 32-byte runs of X^T's rows.  Scales go to
 // s[m / 128][k] (the activation-scale layout of X^T).
 // ---------------------------------------------------------------------------
-constexpr int kTStages = 3;
-constexpr int kTTileBytes = 128 * 128 * 2;
-constexpr int kTSmem = kTStages * kTTileBytes + kTStages * 8 + 4 * 64 * 4 + 1024;
+constexpr int kTRingBytes = 96 * 1024;
+template <bool FROM_FP8>
+struct TQuant {
+  static constexpr int kTileBytes = 128 * 128 * (FROM_FP8 ? 1 : 2);
+  static constexpr int kStages = kTRingBytes / kTileBytes;
+  static constexpr int kScaleBytes = FROM_FP8 ? 128 * 4 : 0;  // per stage: the tile's row scales
+  static constexpr int kOffBars = kTRingBytes + kStages * kScaleBytes;
+  static constexpr int kSmem = kOffBars + kStages * 8 + 4 * 64 * 4 + 1024;
+};
+
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 // Gather 8 BF16 values of one column (low or high halves of 8 packed pairs).
 __device__ __forceinline__ uint4 column8(const uint32_t* r, bool high) {
@@ -41,17 +61,32 @@ __device__ __forceinline__ uint4 column8(const uint32_t* r, bool high) {
                     __byte_perm(r[6], r[7], sel));
 }
 
+template <bool FROM_FP8>
 __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                    int64_t MB, int64_t KB, uint4* __restrict__ q,
                                                                    int64_t ldq_v, float* __restrict__ s,
-                                                                   int64_t ld_s, unsigned* status,
+                                                                   int64_t ld_s, const float* __restrict__ sa,
+                                                                   int64_t ld_sa, unsigned* status,
                                                                    uint64_t timeout_ns) {
+  constexpr int kTStages = TQuant<FROM_FP8>::kStages;
+  constexpr int kTTileBytes = TQuant<FROM_FP8>::kTileBytes;
+  constexpr int kScaleBytes = TQuant<FROM_FP8>::kScaleBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const uint32_t bar_full = base + kTStages * kTTileBytes;
-  uint32_t* quarter_max = reinterpret_cast<uint32_t*>(smem + kTStages * kTTileBytes + kTStages * 8);  // [4][64]
+  const uint32_t bar_full = base + TQuant<FROM_FP8>::kOffBars;
+  uint32_t* quarter_max = reinterpret_cast<uint32_t*>(smem + TQuant<FROM_FP8>::kOffBars + kTStages * 8);  // [4][64]
+  // load of tile t into stage st: the tile by TMA, plus (cached input) its
+  // 128 row scales sa[kb][128 mb ..] by a bulk copy, on one barrier
+  auto issue = [&](int st, int64_t t) {
+    mbar_arrive_expect_tx(bar_full + 8 * st, kTTileBytes + kScaleBytes);
+    tma_load_2d(base + st * kTTileBytes, &tmX, bar_full + 8 * st, static_cast<int32_t>((t % KB) * 128),
+                static_cast<int32_t>((t / KB) * 128));
+    if constexpr (FROM_FP8)
+      bulk_load_1d(base + kTRingBytes + st * kScaleBytes, sa + (t % KB) * ld_sa + (t / KB) * 128, kScaleBytes,
+                   bar_full + 8 * st);
+  };
 
   const int64_t tiles = MB * KB;
   const int64_t first = blockIdx.x, stride = gridDim.x;
@@ -65,9 +100,7 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
     for (int st = 0; st < kTStages; ++st) {
       const int64_t t = first + st * stride;
       if (t >= tiles) break;
-      mbar_arrive_expect_tx(bar_full + 8 * st, kTTileBytes);
-      tma_load_2d(base + st * kTTileBytes, &tmX, bar_full + 8 * st, static_cast<int32_t>((t % KB) * 128),
-                  static_cast<int32_t>((t / KB) * 128));
+      issue(st, t);
     }
   }
   __syncthreads();
@@ -76,6 +109,7 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
   for (int64_t t = first; t < tiles; t += stride, ++i) {
     const int st = static_cast<int>(i % kTStages);
     const uint32_t parity = static_cast<uint32_t>((i / kTStages) & 1);
+    const int64_t mb = t / KB, kb = t % KB;
     const bool landed = mbar_wait(bar_full + 8 * st, parity, nullptr, timeout_ns);
     if (!__syncthreads_and(landed)) {
       if (threadIdx.x == 0) {
@@ -89,11 +123,20 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
       }
       return;
     }
-    const int64_t mb = t / KB, kb = t % KB;
     const uint8_t* tile = smem + st * kTTileBytes;
-    uint32_t r[32];  // rows 32 rq + j, columns 2cp (low half) and 2cp + 1 (high half)
+    uint32_t r[32];  // BF16 pairs of rows 32 rq + j, columns 2cp (low half) and 2cp + 1 (high half)
+    if constexpr (FROM_FP8) {
+      const float* row_s = reinterpret_cast<const float*>(smem + kTRingBytes + st * kScaleBytes) + 32 * rq;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = *reinterpret_cast<const uint32_t*>(tile + (32 * rq + j) * 256 + cp * 4);
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t c2 = *reinterpret_cast<const uint16_t*>(tile + (32 * rq + j) * 128 + cp * 2);
+        const float sj = row_s[j];
+        r[j] = bf16x2_rn(__fmul2_rn(e4m3x2_to_f32x2(c2), make_float2(sj, sj)));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = *reinterpret_cast<const uint32_t*>(tile + (32 * rq + j) * 256 + cp * 4);
+    }
     uint32_t m = r[0] & 0x7FFF7FFFu;
 #pragma unroll
     for (int j = 1; j < 32; ++j) m = max_pairs(m, r[j] & 0x7FFF7FFFu);
@@ -101,11 +144,7 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
     __syncthreads();  // quarter maxima visible; stage st fully read into registers
     if (threadIdx.x == 0) {
       const int64_t tn = t + kTStages * stride;
-      if (tn < tiles) {
-        mbar_arrive_expect_tx(bar_full + 8 * st, kTTileBytes);
-        tma_load_2d(base + st * kTTileBytes, &tmX, bar_full + 8 * st, static_cast<int32_t>((tn % KB) * 128),
-                    static_cast<int32_t>((tn / KB) * 128));
-      }
+      if (tn < tiles) issue(st, tn);
     }
     m = max_pairs(max_pairs(quarter_max[cp], quarter_max[64 + cp]),
                   max_pairs(quarter_max[128 + cp], quarter_max[192 + cp]));
@@ -188,20 +227,38 @@ constexpr int64_t kMaxGridY = 65535;
 
 }  // namespace
 
-cudaError_t launch_quant_act_1x128_t(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
-                                     void* qt, int64_t ldqt, float* st, int64_t ld_st, cudaStream_t stream) {
+template <bool FROM_FP8>
+cudaError_t launch_quant_t(const DeviceInfo& dev, const CUtensorMap& tmX, int64_t M, int64_t K, void* qt,
+                           int64_t ldqt, float* st, int64_t ld_st, const float* sa, int64_t ld_sa,
+                           cudaStream_t stream) {
   const int64_t MB = M / 128, KB = K / 128;
-  CUtensorMap tmX;
-  if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(quant_act_1x128_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+  constexpr int kSmem = TQuant<FROM_FP8>::kSmem;
+  cudaError_t e =
+      cudaFuncSetAttribute(quant_act_1x128_t_kernel<FROM_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = MB * KB;
   const int64_t resident = static_cast<int64_t>(dev.num_sms) * 2;
   const int grid = static_cast<int>(tiles < resident ? tiles : resident);
-  quant_act_1x128_t_kernel<<<grid, 256, kTSmem, stream>>>(tmX, MB, KB, static_cast<uint4*>(qt), ldqt / 16, st,
-                                                          ld_st, dev.status, wait_timeout_ns());
+  quant_act_1x128_t_kernel<FROM_FP8><<<grid, 256, kSmem, stream>>>(
+      tmX, MB, KB, static_cast<uint4*>(qt), ldqt / 16, st, ld_st, sa, ld_sa, dev.status, wait_timeout_ns());
   return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_1x128_t(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     void* qt, int64_t ldqt, float* st, int64_t ld_st, cudaStream_t stream) {
+  CUtensorMap tmX;
+  if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  return launch_quant_t<false>(dev, tmX, M, K, qt, ldqt, st, ld_st, nullptr, 0, stream);
+}
+
+cudaError_t launch_requant_act_1x128_t(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
+                                       int64_t ld_sa, int64_t M, int64_t K, void* qt, int64_t ldqt, float* st,
+                                       int64_t ld_st, cudaStream_t stream) {
+  CUtensorMap tmX;
+  if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  return launch_quant_t<true>(dev, tmX, M, K, qt, ldqt, st, ld_st, sa, ld_sa, stream);
 }
 
 cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,

@@ -68,6 +68,12 @@ cudaError_t launch_blockscaled_gemm_rowscaled(const DeviceInfo& dev, const void*
 cudaError_t launch_quant_act_1x128_t(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
                                      void* qt, int64_t ldqt, float* st, int64_t ld_st, cudaStream_t stream);
 
+// The same from X's FP8 cache (1x128 codes [M, K], stride ldqa; scales
+// sa[kb * ld_sa + m]): each value is dequantised to BF16 first.
+cudaError_t launch_requant_act_1x128_t(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
+                                       int64_t ld_sa, int64_t M, int64_t K, void* qt, int64_t ldqt, float* st,
+                                       int64_t ld_st, cudaStream_t stream);
+
 cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
                                             const float* sw, void* qt, int64_t ldqt, float* swt,
                                             cudaStream_t stream);

@@ -119,22 +119,6 @@ __global__ void __launch_bounds__(256, 3) quant_weight_128x128_kernel(const uint
 // blocks, y over N blocks); thread t handles 16 codes (one 16-byte chunk) of
 // rows (t / 8) + 32 i, i = 0..3.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 c;\n\t"
-      "cvt.u16.u32 c, %1;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
-      : "=r"(h2)
-      : "r"(two_codes));
-  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
-  return __half22float2(h);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_rn(float2 v) {
-  const __nv_bfloat162 b = __float22bfloat162_rn(v);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-
 // 4 codes (one 32-bit word) -> 4 BF16 values (two 32-bit words).
 __device__ __forceinline__ uint2 dequant4(uint32_t codes, float2 s2) {
   const float2 lo = __fmul2_rn(e4m3x2_to_f32x2(codes & 0xFFFFu), s2);

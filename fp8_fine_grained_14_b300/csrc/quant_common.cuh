@@ -6,12 +6,33 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cstdint>
 
 #include "ptx.cuh"
 
 namespace fp8bs {
+
+// Two E4M3 codes (the low 16 bits; the lower byte is the first value) ->
+// their exact values in FP32: E4M3 values are exact in FP16, so the pair is
+// widened with the hardware e4m3x2 -> f16x2 conversion.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\t"
+      "cvt.u16.u32 c, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "r"(two_codes));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  return __half22float2(h);
+}
+
+// Two FP32 values -> a packed BF16 pair, each rounded to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_rn(float2 v) {
+  const __nv_bfloat162 b = __float22bfloat162_rn(v);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
 
 // fl32(1 / 448), the float32 nearest to 1/448.
 constexpr float kInv448 = 0x1.24924ap-9f;

@@ -175,6 +175,24 @@ fp8bs_status fp8_quant_act_1x128_t(const void* x_bf16, int64_t M, int64_t K, int
                                    void* qt, int64_t ldqt, float* st, int64_t ld_st, cudaStream_t stream);
 
 /*
+ * fp8_quant_act_1x128_t with X taken from its FP8 cache: the forward's 1x128
+ * codes and scales of X, kept for the backward pass instead of BF16 X
+ * ("The Definitive Information To Deepseek", paragraph 2).  Each cached value
+ * is dequantised to BF16, x = bf16_rn(fl32(dec(qa[m, k]) * sa[kb][m])) (the
+ * conversion of fp8_dequant_weight_128x128 with the 1x128 grouping), and the
+ * result is quantised on 1x128 tiles of X^T exactly as fp8_quant_act_1x128_t
+ * does; the BF16 values never reach HBM.
+ *   qa : [M, K] E4M3 codes, row stride ldqa (bytes, % 16 == 0).
+ *   sa : [K/128, ld_sa] FP32 scales, sa[kb * ld_sa + m] (ld_sa >= M,
+ *        ld_sa % 4 == 0, 16-byte aligned) -- fp8_quant_act_1x128's layout.
+ *   qt, st : as fp8_quant_act_1x128_t.
+ * M % 128 == 0 and K % 128 == 0 (FP8BS_ERR_UNSUPPORTED_SHAPE otherwise).
+ */
+fp8bs_status fp8_requant_act_1x128_t(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                     int64_t M, int64_t K, void* qt, int64_t ldqt, float* st, int64_t ld_st,
+                                     cudaStream_t stream);
+
+/*
  * Codes and block scales of W^T from those of W [N, K]: a 128x128 block is
  * a block either way round ("Figure 7 (a)" item (2)), so nothing is
  * requantised.

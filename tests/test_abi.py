@@ -130,3 +130,18 @@ def test_grouped_validation(lib, args, expect):
 ])
 def test_gemm_residual_validation(lib, args, expect):
     assert lib.fp8_blockscaled_gemm_residual(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 128, A16, 128, 100, 128, A16, 128, A16, 128, None), 3),        # M % 128
+    ((A16, 128, A16, 128, 128, 100, A16, 128, A16, 128, None), 3),        # K % 128
+    ((A16, 128, A16, 64, 128, 128, A16, 128, A16, 128, None), 1),         # ld_sa < M
+    ((A16, 64, A16, 128, 128, 128, A16, 128, A16, 128, None), 1),         # ldqa < K
+    ((None, 128, A16, 128, 128, 128, A16, 128, A16, 128, None), 1),       # null codes
+    ((A16, 128, P(0x10004), 128, 128, 128, A16, 128, A16, 128, None), 2),  # scales not 16-byte aligned
+    ((A16, 136, A16, 128, 128, 128, A16, 128, A16, 128, None), 2),        # ldqa % 16
+    ((A16, 128, A16, 130, 128, 128, A16, 128, A16, 128, None), 2),        # ld_sa % 4
+    ((A16, 128, A16, 0, 0, 128, A16, 0, A16, 128, None), 0),              # M == 0
+])
+def test_requant_validation(lib, args, expect):
+    assert lib.fp8_requant_act_1x128_t(*args) == expect
