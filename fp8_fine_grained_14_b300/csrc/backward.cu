@@ -36,13 +36,14 @@ namespace {
 // values and writes them as two 32-byte runs of X^T's rows.  Scales go to
 // s[m / 128][k] (the activation-scale layout of X^T).
 // ---------------------------------------------------------------------------
-constexpr int kTRingBytes = 96 * 1024;
 template <bool FROM_FP8>
 struct TQuant {
+  static constexpr int kCtasPerSm = FROM_FP8 ? 3 : 2;
+  static constexpr int kRingBytes = (FROM_FP8 ? 64 : 96) * 1024;
   static constexpr int kTileBytes = 128 * 128 * (FROM_FP8 ? 1 : 2);
-  static constexpr int kStages = kTRingBytes / kTileBytes;
+  static constexpr int kStages = kRingBytes / kTileBytes;
   static constexpr int kScaleBytes = FROM_FP8 ? 128 * 4 : 0;  // per stage: the tile's row scales
-  static constexpr int kOffBars = kTRingBytes + kStages * kScaleBytes;
+  static constexpr int kOffBars = kRingBytes + kStages * kScaleBytes;
   static constexpr int kSmem = kOffBars + kStages * 8 + 4 * 64 * 4 + 1024;
 };
 
@@ -62,7 +63,7 @@ __device__ __forceinline__ uint4 column8(const uint32_t* r, bool high) {
 }
 
 template <bool FROM_FP8>
-__global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_constant__ CUtensorMap tmX,
+__global__ void __launch_bounds__(256, TQuant<FROM_FP8>::kCtasPerSm) quant_act_1x128_t_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                    int64_t MB, int64_t KB, uint4* __restrict__ q,
                                                                    int64_t ldq_v, float* __restrict__ s,
                                                                    int64_t ld_s, const float* __restrict__ sa,
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
     tma_load_2d(base + st * kTTileBytes, &tmX, bar_full + 8 * st, static_cast<int32_t>((t % KB) * 128),
                 static_cast<int32_t>((t / KB) * 128));
     if constexpr (FROM_FP8)
-      bulk_load_1d(base + kTRingBytes + st * kScaleBytes, sa + (t % KB) * ld_sa + (t / KB) * 128, kScaleBytes,
+      bulk_load_1d(base + TQuant<FROM_FP8>::kRingBytes + st * kScaleBytes, sa + (t % KB) * ld_sa + (t / KB) * 128, kScaleBytes,
                    bar_full + 8 * st);
   };
 
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
     const uint8_t* tile = smem + st * kTTileBytes;
     uint32_t r[32];  // BF16 pairs of rows 32 rq + j, columns 2cp (low half) and 2cp + 1 (high half)
     if constexpr (FROM_FP8) {
-      const float* row_s = reinterpret_cast<const float*>(smem + kTRingBytes + st * kScaleBytes) + 32 * rq;
+      const float* row_s = reinterpret_cast<const float*>(smem + TQuant<FROM_FP8>::kRingBytes + st * kScaleBytes) + 32 * rq;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const uint32_t c2 = *reinterpret_cast<const uint16_t*>(tile + (32 * rq + j) * 128 + cp * 2);
@@ -163,7 +164,8 @@ __global__ void __launch_bounds__(256, 2) quant_act_1x128_t_kernel(const __grid_
     dst_hi[0] = make_uint4(b0.x, b0.y, b1.x, b1.y);
     dst_hi[1] = make_uint4(b2.x, b2.y, b3.x, b3.y);
     if (rq == 0) *reinterpret_cast<float2*>(s + mb * ld_s + k0) = make_float2(g_lo.s, g_hi.s);
-    __syncthreads();  // quarter_max is rewritten for the next tile
+    // quarter_max is rewritten only after the next tile's __syncthreads_and,
+    // which every thread reaches after its reads above
   }
 }
 
@@ -237,7 +239,7 @@ cudaError_t launch_quant_t(const DeviceInfo& dev, const CUtensorMap& tmX, int64_
       cudaFuncSetAttribute(quant_act_1x128_t_kernel<FROM_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int64_t tiles = MB * KB;
-  const int64_t resident = static_cast<int64_t>(dev.num_sms) * 2;
+  const int64_t resident = static_cast<int64_t>(dev.num_sms) * TQuant<FROM_FP8>::kCtasPerSm;
   const int grid = static_cast<int>(tiles < resident ? tiles : resident);
   quant_act_1x128_t_kernel<FROM_FP8><<<grid, 256, kSmem, stream>>>(
       tmX, MB, KB, static_cast<uint4*>(qt), ldqt / 16, st, ld_st, sa, ld_sa, dev.status, wait_timeout_ns());
