@@ -669,6 +669,13 @@ def run_rows(args):
     ydec = torch.empty((64, N), dtype=torch.bfloat16, device=dev)
     emit("a7 decode GEMM", f"64x{N}x{K}, W pre-quantised",
          lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm(qdec, sdec, qw, sw, y=ydec)), gemm_bytes(64, N, K), "GB/s")
+    wpk = fb.fp8_pack_weight_128x128(qw)
+    emit("a7 decode GEMM, packed W", f"64x{N}x{K}, W pre-quantised and packed",
+         lambda: _time_kernel(lambda: fb.fp8_blockscaled_gemm_packed(qdec, sdec, wpk, sw, y=ydec)),
+         gemm_bytes(64, N, K), "GB/s")
+    emit("a7 weight pack", f"W codes [{N},{K}]",
+         lambda: _time_kernel(lambda: fb.fp8_pack_weight_128x128(qw, wp=wpk)), 2 * N * K, "GB/s")
+    del wpk
     # grouped (MoE): codes and scales drawn directly (the GEMM's inputs)
     cg = workloads.CONFIGS["grouped"]
     routes = torch.multinomial(torch.ones(cg["tokens"], cg["G"]), cg["topk"], replacement=False, generator=gc)

@@ -18,6 +18,8 @@ _API = (
     "fp8_dequant_weight_128x128",
     "fp8_quant_act_1x128_t",
     "fp8_requant_act_1x128_t",
+    "fp8_pack_weight_128x128",
+    "fp8_blockscaled_gemm_packed",
     "fp8_transpose_weight_128x128",
     "fp8_blockscaled_gemm_rowscaled",
     "linear_backward",

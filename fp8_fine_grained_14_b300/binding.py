@@ -39,6 +39,8 @@ EXPORTS = {
     "fp8_dequant_weight_128x128": [_p, _i64, _i64, _i64, _p, _p, _i64, _p],
     "fp8_quant_act_1x128_t": [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
     "fp8_requant_act_1x128_t": [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p],
+    "fp8_pack_weight_128x128": [_p, _i64, _i64, _i64, _p, _p],
+    "fp8_blockscaled_gemm_packed": [_p, _i64, _p, _i64, _p, _p, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_quant_per_token": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
     "fp8_quant_per_channel": [_p, _i64, _i64, _i64, _p, _i64, _p, _p],
     "fp8bs_e5m6_encode_bf16": [_p, _i64, _p, _p],
@@ -290,6 +292,43 @@ def fp8_requant_act_1x128_t(qa, sa, qt=None, st=None, stream=None):
                                          qt.stride(0), _ptr(st), st.stride(0), _stream(stream))
     _check("fp8_requant_act_1x128_t", status)
     return qt, st
+
+
+def fp8_pack_weight_128x128(qw, wp=None, stream=None):
+    """qw uint8 [N, K] -> wp uint8 [N/128, K/128, 16384]: each 128x128 block
+    as the 128-byte-swizzled image a GEMM stage holds (for
+    fp8_blockscaled_gemm_packed)."""
+    _require(qw, torch.uint8, "qw", 2)
+    N, K = qw.shape
+    if wp is None:
+        wp = torch.empty((N // 128, K // 128, 128 * 128), dtype=torch.uint8, device=qw.device)
+    if wp.dtype != torch.uint8 or not wp.is_contiguous() or wp.numel() != N * K:
+        raise ValueError("wp must be a contiguous uint8 tensor of N*K bytes")
+    _check("fp8_pack_weight_128x128", lib.fp8_pack_weight_128x128(_ptr(qw), N, K, qw.stride(0), _ptr(wp),
+                                                                  _stream(stream)))
+    return wp
+
+
+def fp8_blockscaled_gemm_packed(qa, sa, wp, sw, y=None, stream=None):
+    """fp8_blockscaled_gemm with B as packed tiles wp [N/128, K/128, 16384]
+    (fp8_pack_weight_128x128); Y BF16 [M, N], bit for bit the same."""
+    _require(qa, torch.uint8, "qa", 2)
+    _require(sa, torch.float32, "sa", 2)
+    if wp.dim() != 3 or wp.shape[2] != 128 * 128 or not wp.is_contiguous():
+        raise ValueError("wp must be [N/128, K/128, 16384] contiguous")
+    M, K = qa.shape
+    N = wp.shape[0] * 128
+    if wp.shape[1] * 128 != K:
+        raise ValueError("wp and qa disagree on K")
+    if not sw.is_contiguous():
+        raise ValueError("sw must be contiguous")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    _require(y, torch.bfloat16, "y", 2)
+    st = lib.fp8_blockscaled_gemm_packed(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(wp), _ptr(sw), _ptr(y),
+                                         y.stride(0), M, N, K, _stream(stream))
+    _check("fp8_blockscaled_gemm_packed", st)
+    return y
 
 
 def fp8_transpose_weight_128x128(qw, sw, qwt=None, swt=None, stream=None):

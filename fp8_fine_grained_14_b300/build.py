@@ -16,7 +16,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["api.cu", "quant.cu", "backward.cu", "variants.cu", "gemm.cu"]
+SOURCES = ["api.cu", "quant.cu", "backward.cu", "variants.cu", "gemm.cu", "pack.cu"]
 LIB = os.path.join(HERE, "libfp8bs.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -329,6 +329,41 @@ fp8bs_status fp8_quant_act_1x128_t(const void* x_bf16, int64_t M, int64_t K, int
   return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_quant_act_1x128_t launch", e);
 }
 
+fp8bs_status fp8_pack_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, void* wp,
+                                      cudaStream_t stream) {
+  if (N < 0 || K < 0 || ldq < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldq < K) return FP8BS_ERR_INVALID_ARG;
+  if (qw == nullptr || wp == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qw) || !aligned16(wp) || ldq % 16 != 0) return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_pack_weight_128x128(*dev, qw, N, K, ldq, wp, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_pack_weight_128x128 launch", e);
+}
+
+fp8bs_status fp8_blockscaled_gemm_packed(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                         const void* wp, const float* sw, void* y_bf16, int64_t ldy, int64_t M,
+                                         int64_t N, int64_t K, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || ldqa < 0 || ld_sa < 0 || ldy < 0) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (ldqa < K || ldy < N || ld_sa < M) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0) return FP8BS_OK;
+  if (qa == nullptr || sa == nullptr || wp == nullptr || sw == nullptr || y_bf16 == nullptr)
+    return FP8BS_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(wp) || !aligned16(sw) || !aligned16(y_bf16) || ldqa % 16 != 0 ||
+      ld_sa % 4 != 0 || ldy % 8 != 0)
+    return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_blockscaled_gemm_packed(*dev, qa, ldqa, sa, ld_sa, wp, sw, y_bf16, ldy, false, M, N, K, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("fp8_blockscaled_gemm_packed launch", e);
+}
+
 fp8bs_status fp8_requant_act_1x128_t(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, int64_t M,
                                      int64_t K, void* qt, int64_t ldqt, float* st, int64_t ld_st,
                                      cudaStream_t stream) {

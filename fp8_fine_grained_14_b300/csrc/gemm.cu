@@ -108,7 +108,21 @@ struct Params {
   // result before the output rounding; null when there is none.
   const uint16_t* res;
   int64_t ldr;
+  // Dense single-CTA tiles only: B as packed 128x128 tiles, each the 16 KB
+  // shared-memory image of its stage (see fp8_pack_weight_128x128), loaded
+  // by one bulk copy per tile instead of a tensor-map load; null otherwise.
+  const uint8_t* b_packed;
 };
+
+constexpr uint32_t kPackedTileBytes = 128 * 128;
+
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 // Bring the 128-byte line holding `ptr` into L2 (a hint; no fault on any
 // address the caller may also load).
@@ -347,7 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t full = bar_full + 8 * stage;
             mbar_arrive_expect_tx(full, kStageTx);
             tma_load_2d(a_dst, &tmA, full, kb * BK, a_row);
-            tma_load_2d(b_dst, &tmB, full, kb * BK, b_row);
+            if (!GROUPED && p.b_packed != nullptr) {
+              // BN / 128 packed tiles (rows b_row.., chunk kb), each one
+              // contiguous 16 KB image of its part of the stage
+              const uint8_t* src = p.b_packed + (static_cast<int64_t>(b_row / 128) * p.KB + kb) * kPackedTileBytes;
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                bulk_load_1d(b_dst + h * kPackedTileBytes, src + static_cast<int64_t>(h) * p.KB * kPackedTileBytes,
+                             kPackedTileBytes, full);
+            } else {
+              tma_load_2d(b_dst, &tmB, full, kb * BK, b_row);
+            }
           } else {
             // the leader expects the whole pair's bytes; each CTA loads its
             // own A rows and its half of B and credits the leader's barrier
@@ -847,6 +871,7 @@ Params make_params(const DeviceInfo& dev, const float* sa, int64_t ld_sa, const 
   p.ld_sb = 0;
   p.res = nullptr;
   p.ldr = 0;
+  p.b_packed = nullptr;
   p.y = y;
   p.ldy = ldy;
   p.M = static_cast<int32_t>(M);
@@ -924,6 +949,29 @@ cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64
   return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes)
                : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch,
                                             scratch_bytes);
+}
+
+cudaError_t launch_blockscaled_gemm_packed(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
+                                           int64_t ld_sa, const void* wp, const float* sw, void* y, int64_t ldy,
+                                           bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+  // Single-CTA tiles only (a pair's B half would credit the peer's barrier).
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  const bool wide = (N % 256 == 0) && m_tiles * (N / 256) >= dev.num_sms;
+  const Shape shape = wide ? Shape::kWide : (M <= BM / 2 ? Shape::kNarrowHalfA : Shape::kNarrow);
+  const int BN = wide ? 256 : 128;
+  const int out_bytes = y_f32 ? 4 : 2;
+  const uint32_t a_rows = shape == Shape::kNarrowHalfA ? BM / 2 : BM;
+  CUtensorMap tmA, tmY;
+  if (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, BK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tmY, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M,
+                    ldy * out_bytes, kEpiRowBytes / out_bytes, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const CUtensorMap& tmB = tmA;  // unused: B arrives by bulk copies
+  Params p = make_params(dev, sa, ld_sa, sw, y, ldy, M, N, K, nullptr, 1);
+  p.b_packed = static_cast<const uint8_t*>(wp);
+  const int64_t cluster_tiles = m_tiles * (N / BN);
+  return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream)
+               : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream);
 }
 
 cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,

@@ -49,6 +49,17 @@ cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64
                                     float* scratch = nullptr, size_t scratch_bytes = 0, const void* res = nullptr,
                                     int64_t ldr = 0);
 
+// As launch_blockscaled_gemm with B as packed 128x128 tiles wp[N/128][K/128]
+// (fp8_pack_weight_128x128's layout); single-CTA tile shapes only.
+cudaError_t launch_blockscaled_gemm_packed(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
+                                           int64_t ld_sa, const void* wp, const float* sw, void* y, int64_t ldy,
+                                           bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+// Codes W [N, K] -> packed tiles wp[N/128][K/128][128 x 128 bytes], each the
+// 128B-swizzled K-major image that a GEMM stage holds.
+cudaError_t launch_pack_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
+                                       void* wp, cudaStream_t stream);
+
 cudaError_t launch_blockscaled_grouped_gemm(const DeviceInfo& dev, int32_t G, const int32_t* offsets,
                                             int64_t M_total, const void* qa, int64_t ldqa, const float* sa,
                                             int64_t ld_sa, const void* qw, const float* sw, void* y, int64_t ldy,

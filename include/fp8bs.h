@@ -163,6 +163,33 @@ fp8bs_status fp8_dequant_weight_128x128(const void* qw, int64_t N, int64_t K, in
  * ------------------------------------------------------------------------ */
 
 /*
+ * Weight codes in the GEMM's stage layout, for weight-streaming
+ * (decode-shaped) GEMMs.  The codes and block scales stay those of
+ * fp8_quant_weight_128x128 ("Figure 7 (a)" item (2)); only the byte order
+ * changes: packed tile (nb, kb) is 16384 contiguous bytes at
+ * wp + (nb * K/128 + kb) * 16384, holding rows 128 nb + r (r < 128) and
+ * columns 128 kb + c (c < 128) of qw with byte (r, c) at
+ *     128 r + 16 ((c / 16) XOR (r % 8)) + (c % 16),
+ * the 128-byte-swizzled K-major image that a GEMM stage holds.
+ *   qw : [N, K] codes, row stride ldq (bytes, % 16 == 0).
+ *   wp : N * K bytes out, 16-byte aligned.
+ * N % 128 == 0 and K % 128 == 0.
+ */
+fp8bs_status fp8_pack_weight_128x128(const void* qw, int64_t N, int64_t K, int64_t ldq, void* wp,
+                                     cudaStream_t stream);
+
+/*
+ * fp8_blockscaled_gemm with B given as packed tiles (fp8_pack_weight_128x128):
+ * the same Y, bit for bit, but every B stage arrives as one contiguous bulk
+ * copy.  Meant for skinny M, where streaming the weights is the whole cost;
+ * large grids run on single-CTA tiles (no CTA pairs).  sw as for
+ * fp8_blockscaled_gemm; other arguments and errors likewise.
+ */
+fp8bs_status fp8_blockscaled_gemm_packed(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
+                                         const void* wp, const float* sw, void* y_bf16, int64_t ldy,
+                                         int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
  * 1x128 quantisation of X^T for X [M, K] BF16 (row stride ldx): each run of
  * 128 rows of one column is a group.
  *   qt : [K, M] E4M3 codes of X^T out, row stride ldqt (bytes, % 16 == 0).

@@ -145,3 +145,26 @@ def test_gemm_residual_validation(lib, args, expect):
 ])
 def test_requant_validation(lib, args, expect):
     assert lib.fp8_requant_act_1x128_t(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 100, 128, 128, A16, None), 3),          # N % 128
+    ((A16, 128, 100, 128, A16, None), 3),          # K % 128
+    ((A16, 128, 128, 64, A16, None), 1),           # ldq < K
+    ((None, 128, 128, 128, A16, None), 1),         # null codes
+    ((A16, 128, 128, 128, P(0x10008), None), 2),   # misaligned output
+    ((A16, 128, 128, 136, A16, None), 2),          # ldq % 16
+])
+def test_pack_validation(lib, args, expect):
+    assert lib.fp8_pack_weight_128x128(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, 128, A16, 4, A16, A16, A16, 128, 1, 100, 128, None), 3),       # N % 128
+    ((A16, 128, A16, 4, A16, A16, A16, 128, 0, 128, 128, None), 0),       # M == 0
+    ((A16, 128, A16, 4, None, A16, A16, 128, 1, 128, 128, None), 1),     # null packed weights
+    ((A16, 128, A16, 4, P(0x10008), A16, A16, 128, 1, 128, 128, None), 2),  # misaligned packed weights
+    ((A16, 128, A16, 4, A16, A16, A16, 120, 1, 128, 128, None), 1),       # ldy < N
+])
+def test_gemm_packed_validation(lib, args, expect):
+    assert lib.fp8_blockscaled_gemm_packed(*args) == expect
