@@ -21,9 +21,15 @@
 //               the TMEM buffer back as soon as the whole chunk has been read
 //               (for 128 columns per warp the FMAs of the first 64 run between
 //               the two loads: accumulators and 128 loaded columns do not fit
-//               in registers together); after the last chunk, BF16 (RNE) ->
-//               swizzled smem -> TMA store (dense) or row-masked coalesced
-//               stores (grouped)
+//               in registers together); after the last chunk, BF16 (RNE) or
+//               FP32 -> swizzled smem -> TMA store (dense) or row-masked
+//               coalesced stores (grouped).  A template variant (RES) adds a
+//               BF16 residual to the FP32 result before the rounding.
+//
+// B normally arrives by a tensor-map load of BN/CG rows x 128 bytes per stage.
+// With packed weights (Params::b_packed, single-CTA tiles) each 128-row part
+// of a stage is already stored as its 16 KB swizzled image and arrives by one
+// contiguous bulk copy.
 //
 // Wide tiles run on CTA pairs (CG = 2, a cluster of two CTAs on two SMs):
 // the pair computes a 256 x 256 tile with tcgen05 cta_group::2 MMAs issued by
