@@ -94,6 +94,24 @@ def _require(t, dtype, name, ndim):
         raise ValueError(f"{name} must have unit stride along its last dimension")
 
 
+def _require_min(t, dtype, name, rows, cols):
+    """A 2-D buffer the library reads or writes through its row stride: it
+    must hold at least `rows` rows of `cols` elements, since the C ABI sees
+    only the pointer and the stride."""
+    _require(t, dtype, name, 2)
+    if t.shape[0] < rows or t.shape[1] < cols:
+        raise ValueError(f"{name} must be at least [{rows}, {cols}], got {list(t.shape)}")
+
+
+def _require_count(t, name, count, dtype=torch.float32):
+    """A contiguous buffer the library indexes densely (block scales, per-row
+    or per-column scales): at least `count` elements."""
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    if t.numel() < count:
+        raise ValueError(f"{name} must hold at least {count} elements, got {t.numel()}")
+
+
 def ld_sa_for(m: int) -> int:
     """Row stride of the transposed activation-scale matrix: M rounded up to 4."""
     return (m + 3) // 4 * 4
@@ -110,8 +128,8 @@ def fp8_quant_act_1x128(x, qa=None, sa=None, stream=None):
         qa = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if sa is None:
         sa = torch.empty((K // 128, ld_sa_for(M)), dtype=torch.float32, device=x.device)
-    _require(qa, torch.uint8, "qa", 2)
-    _require(sa, torch.float32, "sa", 2)
+    _require_min(qa, torch.uint8, "qa", M, K)
+    _require_min(sa, torch.float32, "sa", K // 128, M)
     st = lib.fp8_quant_act_1x128(_ptr(x), M, K, x.stride(0), _ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0),
                                  _stream(stream))
     _check("fp8_quant_act_1x128", st)
@@ -134,9 +152,8 @@ def fp8_quant_weight_128x128(w, qw=None, sw=None, stream=None):
         qw = torch.empty((N, K), dtype=torch.uint8, device=w.device)
     if sw is None:
         sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
-    _require(qw, torch.uint8, "qw", 2)
-    if not sw.is_contiguous():
-        raise ValueError("sw must be contiguous")
+    _require_min(qw, torch.uint8, "qw", N, K)
+    _require_count(sw, "sw", (N // 128) * (K // 128))
     st = lib.fp8_quant_weight_128x128(_ptr(w), N, K, w.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
                                       _stream(stream))
     _check("fp8_quant_weight_128x128", st)
@@ -156,9 +173,10 @@ def fp8_blockscaled_gemm(qa, sa, qw, sw, y=None, stream=None, out_dtype=torch.bf
         y = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     if y.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("y must be bfloat16 or float32")
-    _require(y, y.dtype, "y", 2)
-    if not sw.is_contiguous():
-        raise ValueError("sw must be contiguous")
+    _require_min(y, y.dtype, "y", M, N)
+    _require_min(qw, torch.uint8, "qw", N, K)
+    _require_min(sa, torch.float32, "sa", K // 128, M)
+    _require_count(sw, "sw", (N // 128) * (K // 128))
     fn = "fp8_blockscaled_gemm" if y.dtype == torch.bfloat16 else "fp8_blockscaled_gemm_f32"
     st = getattr(lib, fn)(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
                           _ptr(y), y.stride(0), M, N, K, _stream(stream))
@@ -180,9 +198,10 @@ def fp8_blockscaled_gemm_residual(qa, sa, qw, sw, residual, y=None, stream=None)
         raise ValueError("residual must be [M, N]")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    _require(y, torch.bfloat16, "y", 2)
-    if not sw.is_contiguous():
-        raise ValueError("sw must be contiguous")
+    _require_min(y, torch.bfloat16, "y", M, N)
+    _require_min(qw, torch.uint8, "qw", N, K)
+    _require_min(sa, torch.float32, "sa", K // 128, M)
+    _require_count(sw, "sw", (N // 128) * (K // 128))
     st = lib.fp8_blockscaled_gemm_residual(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0),
                                            _ptr(sw), _ptr(residual), residual.stride(0), _ptr(y), y.stride(0),
                                            M, N, K, _stream(stream))
@@ -202,9 +221,10 @@ def fp8_blockscaled_gemm_noalloc(qa, sa, qw, sw, y=None, stream=None):
     N = qw.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    _require(y, torch.bfloat16, "y", 2)
-    if not sw.is_contiguous():
-        raise ValueError("sw must be contiguous")
+    _require_min(y, torch.bfloat16, "y", M, N)
+    _require_min(qw, torch.uint8, "qw", N, K)
+    _require_min(sa, torch.float32, "sa", K // 128, M)
+    _require_count(sw, "sw", (N // 128) * (K // 128))
     st = lib.fp8_blockscaled_gemm_noalloc(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qw), qw.stride(0),
                                           _ptr(sw), _ptr(y), y.stride(0), M, N, K, _stream(stream))
     _check("fp8_blockscaled_gemm_noalloc", st)
@@ -228,7 +248,12 @@ def fp8_blockscaled_grouped_gemm(group_offsets, m_total, qa, sa, qw, sw, y=None,
         y = torch.empty((m_total, N), dtype=out_dtype, device=qa.device)
     if y.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("y must be bfloat16 or float32")
-    _require(y, y.dtype, "y", 2)
+    _require_min(y, y.dtype, "y", m_total, N)
+    _require_min(qa, torch.uint8, "qa", m_total, K)
+    _require_min(sa, torch.float32, "sa", K // 128, m_total)
+    _require_count(sw, "sw", G * (N // 128) * (K // 128))
+    if group_offsets.numel() != G + 1:
+        raise ValueError("group_offsets must hold G + 1 offsets")
     fn = "fp8_blockscaled_grouped_gemm" if y.dtype == torch.bfloat16 else "fp8_blockscaled_grouped_gemm_f32"
     st = getattr(lib, fn)(G, _ptr(group_offsets), int(m_total), _ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0),
                           _ptr(qw), _ptr(sw), _ptr(y), y.stride(0), N, K, _stream(stream))
@@ -249,9 +274,8 @@ def fp8_dequant_weight_128x128(qw, sw, y=None, stream=None):
     N, K = qw.shape
     if y is None:
         y = torch.empty((N, K), dtype=torch.bfloat16, device=qw.device)
-    _require(y, torch.bfloat16, "y", 2)
-    if not sw.is_contiguous() or sw.dtype != torch.float32:
-        raise ValueError("sw must be a contiguous float32 tensor")
+    _require_min(y, torch.bfloat16, "y", N, K)
+    _require_count(sw, "sw", (N // 128) * (K // 128))
     st = lib.fp8_dequant_weight_128x128(_ptr(qw), N, K, qw.stride(0), _ptr(sw), _ptr(y), y.stride(0), _stream(stream))
     _check("fp8_dequant_weight_128x128", st)
     return y
@@ -266,8 +290,8 @@ def fp8_quant_act_1x128_t(x, qt=None, st=None, stream=None):
         qt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
     if st is None:
         st = torch.empty((M // 128, ld_sa_for(K)), dtype=torch.float32, device=x.device)
-    _require(qt, torch.uint8, "qt", 2)
-    _require(st, torch.float32, "st", 2)
+    _require_min(qt, torch.uint8, "qt", K, M)
+    _require_min(st, torch.float32, "st", M // 128, K)
     status = lib.fp8_quant_act_1x128_t(_ptr(x), M, K, x.stride(0), _ptr(qt), qt.stride(0), _ptr(st), st.stride(0),
                                        _stream(stream))
     _check("fp8_quant_act_1x128_t", status)
@@ -286,8 +310,9 @@ def fp8_requant_act_1x128_t(qa, sa, qt=None, st=None, stream=None):
         qt = torch.empty((K, M), dtype=torch.uint8, device=qa.device)
     if st is None:
         st = torch.empty((M // 128, ld_sa_for(K)), dtype=torch.float32, device=qa.device)
-    _require(qt, torch.uint8, "qt", 2)
-    _require(st, torch.float32, "st", 2)
+    _require_min(sa, torch.float32, "sa", K // 128, M)
+    _require_min(qt, torch.uint8, "qt", K, M)
+    _require_min(st, torch.float32, "st", M // 128, K)
     status = lib.fp8_requant_act_1x128_t(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), M, K, _ptr(qt),
                                          qt.stride(0), _ptr(st), st.stride(0), _stream(stream))
     _check("fp8_requant_act_1x128_t", status)
@@ -320,11 +345,11 @@ def fp8_blockscaled_gemm_packed(qa, sa, wp, sw, y=None, stream=None):
     N = wp.shape[0] * 128
     if wp.shape[1] * 128 != K:
         raise ValueError("wp and qa disagree on K")
-    if not sw.is_contiguous():
-        raise ValueError("sw must be contiguous")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    _require(y, torch.bfloat16, "y", 2)
+    _require_min(y, torch.bfloat16, "y", M, N)
+    _require_min(sa, torch.float32, "sa", K // 128, M)
+    _require_count(sw, "sw", (N // 128) * (K // 128))
     st = lib.fp8_blockscaled_gemm_packed(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(wp), _ptr(sw), _ptr(y),
                                          y.stride(0), M, N, K, _stream(stream))
     _check("fp8_blockscaled_gemm_packed", st)
@@ -339,9 +364,9 @@ def fp8_transpose_weight_128x128(qw, sw, qwt=None, swt=None, stream=None):
         qwt = torch.empty((K, N), dtype=torch.uint8, device=qw.device)
     if swt is None:
         swt = torch.empty((K // 128, N // 128), dtype=torch.float32, device=qw.device)
-    _require(qwt, torch.uint8, "qwt", 2)
-    if not sw.is_contiguous() or not swt.is_contiguous():
-        raise ValueError("sw and swt must be contiguous")
+    _require_min(qwt, torch.uint8, "qwt", K, N)
+    _require_count(sw, "sw", (N // 128) * (K // 128))
+    _require_count(swt, "swt", (N // 128) * (K // 128))
     status = lib.fp8_transpose_weight_128x128(_ptr(qw), N, K, qw.stride(0), _ptr(sw), _ptr(qwt), qwt.stride(0),
                                               _ptr(swt), _stream(stream))
     _check("fp8_transpose_weight_128x128", status)
@@ -361,7 +386,10 @@ def fp8_blockscaled_gemm_rowscaled(qa, sa, qb, sb, y=None, stream=None, out_dtyp
         y = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     if y.dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("y must be bfloat16 or float32")
-    _require(y, y.dtype, "y", 2)
+    _require_min(y, y.dtype, "y", M, N)
+    _require_min(qb, torch.uint8, "qb", N, K)
+    _require_min(sa, torch.float32, "sa", K // 128, M)
+    _require_min(sb, torch.float32, "sb", K // 128, N)
     fn = "fp8_blockscaled_gemm_rowscaled" if y.dtype == torch.bfloat16 else "fp8_blockscaled_gemm_rowscaled_f32"
     status = getattr(lib, fn)(_ptr(qa), qa.stride(0), _ptr(sa), sa.stride(0), _ptr(qb), qb.stride(0), _ptr(sb),
                               sb.stride(0), _ptr(y), y.stride(0), M, N, K, _stream(stream))
@@ -375,7 +403,8 @@ def fp8_quant_per_token(x, q=None, s=None, stream=None):
     M, K = x.shape
     q = q if q is not None else torch.empty((M, K), dtype=torch.uint8, device=x.device)
     s = s if s is not None else torch.empty((M,), dtype=torch.float32, device=x.device)
-    _require(q, torch.uint8, "q", 2)
+    _require_min(q, torch.uint8, "q", M, K)
+    _require_count(s, "s", M)
     st = lib.fp8_quant_per_token(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), _stream(stream))
     _check("fp8_quant_per_token", st)
     return q, s
@@ -387,7 +416,8 @@ def fp8_quant_per_channel(x, q=None, s=None, stream=None):
     M, K = x.shape
     q = q if q is not None else torch.empty((M, K), dtype=torch.uint8, device=x.device)
     s = s if s is not None else torch.empty((K,), dtype=torch.float32, device=x.device)
-    _require(q, torch.uint8, "q", 2)
+    _require_min(q, torch.uint8, "q", M, K)
+    _require_count(s, "s", K)
     st = lib.fp8_quant_per_channel(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s), _stream(stream))
     _check("fp8_quant_per_channel", st)
     return q, s
@@ -398,6 +428,7 @@ def e5m6_encode(x, codes=None, stream=None):
     if x.dtype != torch.bfloat16 or not x.is_contiguous() or not x.is_cuda:
         raise TypeError("x must be a contiguous CUDA bfloat16 tensor")
     codes = codes if codes is not None else torch.empty(x.shape, dtype=torch.int16, device=x.device)
+    _require_count(codes, "codes", x.numel(), dtype=torch.int16)
     st = lib.fp8bs_e5m6_encode_bf16(_ptr(x), x.numel(), _ptr(codes), _stream(stream))
     _check("fp8bs_e5m6_encode_bf16", st)
     return codes
@@ -408,6 +439,7 @@ def e5m6_decode(codes, y=None, stream=None):
     if codes.dtype != torch.int16 or not codes.is_contiguous() or not codes.is_cuda:
         raise TypeError("codes must be a contiguous CUDA int16 tensor")
     y = y if y is not None else torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
+    _require_count(y, "y", codes.numel(), dtype=torch.bfloat16)
     st = lib.fp8bs_e5m6_decode_bf16(_ptr(codes), codes.numel(), _ptr(y), _stream(stream))
     _check("fp8bs_e5m6_decode_bf16", st)
     return y
@@ -423,6 +455,10 @@ def fp8_swiglu_quant_act_1x128(gate_up, qa=None, sa=None, h=None, return_h=False
     sa = sa if sa is not None else torch.empty((F // 128, ld_sa_for(M)), dtype=torch.float32, device=gate_up.device)
     if return_h and h is None:
         h = torch.empty((M, F), dtype=torch.bfloat16, device=gate_up.device)
+    _require_min(qa, torch.uint8, "qa", M, F)
+    _require_min(sa, torch.float32, "sa", F // 128, M)
+    if h is not None:
+        _require_min(h, torch.bfloat16, "h", M, F)
     st = lib.fp8_swiglu_quant_act_1x128(_ptr(gate_up), M, F, gate_up.stride(0), _ptr(qa), qa.stride(0), _ptr(sa),
                                         sa.stride(0), _ptr(h), h.stride(0) if h is not None else 0,
                                         _stream(stream))

@@ -125,3 +125,39 @@ def test_grouped_empty_middle_group():
         qw_r, sw_r = oracle.quant_weight_128x128(f32(w[gi]))
         parts.append(oracle.blockscaled_gemm(qa_r[r0:r1], sa_r[:, r0:r1], qw_r, sw_r))
     assert_gemm_close(f32(y), np.concatenate(parts))
+
+
+def test_wrappers_reject_undersized_buffers():
+    """The C ABI sees only pointers and row strides, so the Python wrappers
+    check that every buffer they pass holds the rows, columns or scales the
+    call will touch, and raise before anything is launched."""
+    x = torch.zeros((256, 256), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ValueError):
+        fb.fp8_quant_act_1x128(x, qa=torch.empty((128, 256), dtype=torch.uint8, device=DEV))
+    with pytest.raises(ValueError):
+        fb.fp8_quant_act_1x128(x, sa=torch.empty((2, 128), dtype=torch.float32, device=DEV))
+    qa, sa = fb.fp8_quant_act_1x128(x)
+    qw, sw = fb.fp8_quant_weight_128x128(x)
+    with pytest.raises(ValueError):
+        fb.fp8_blockscaled_gemm(qa, sa, qw, sw[:1].contiguous())
+    with pytest.raises(ValueError):
+        fb.fp8_blockscaled_gemm(qa, sa, qw, sw, y=torch.empty((256, 128), dtype=torch.bfloat16, device=DEV))
+    with pytest.raises(ValueError):
+        fb.fp8_blockscaled_gemm_residual(qa, sa, qw, sw, torch.zeros((256, 256), dtype=torch.bfloat16, device=DEV),
+                                         y=torch.empty((200, 256), dtype=torch.bfloat16, device=DEV))
+    with pytest.raises(ValueError):
+        fb.fp8_transpose_weight_128x128(qw, sw, swt=torch.empty((1, 1), dtype=torch.float32, device=DEV))
+    with pytest.raises(ValueError):
+        fb.fp8_dequant_weight_128x128(qw, sw[:1].contiguous())
+    qw3 = qw.reshape(2, 128, 256)
+    sw3 = sw.reshape(2, 1, 2)
+    with pytest.raises(ValueError):
+        fb.fp8_blockscaled_grouped_gemm(torch.zeros((2,), dtype=torch.int32, device=DEV), 256, qa, sa, qw3, sw3)
+    with pytest.raises(ValueError):
+        fb.fp8_blockscaled_grouped_gemm(torch.zeros((3,), dtype=torch.int32, device=DEV), 300, qa, sa, qw3, sw3)
+    with pytest.raises(ValueError):
+        fb.fp8_requant_act_1x128_t(qa, sa, st=torch.empty((1, 256), dtype=torch.float32, device=DEV))
+    with pytest.raises(ValueError):
+        fb.fp8_quant_per_token(x, s=torch.empty((100,), dtype=torch.float32, device=DEV))
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
