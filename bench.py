@@ -734,7 +734,7 @@ def run_rows(args):
     emit("NEXT4 per-token quant", f"X [{M},{K}]", lambda: _time_kernel(lambda: fb.fp8_quant_per_token(x, q=qpt, s=spt)),
          3 * M * K + 4 * M, "GB/s", lambda: oracle.quant_per_token(xs), 3 * 256 * K, "X[:256]")
     spc = torch.empty((K,), dtype=torch.float32, device=dev)
-    emit("NEXT4 per-channel quant", f"X [{M},{K}] (read twice)",
+    emit("NEXT4 per-channel quant", f"X [{M},{K}], one pass on 8-CTA clusters",
          lambda: _time_kernel(lambda: fb.fp8_quant_per_channel(x, q=qpt, s=spc)), 3 * M * K + 4 * K, "GB/s",
          lambda: oracle.quant_per_channel(xs), 3 * 256 * K, "X[:256]")
     codes = torch.empty((M, K), dtype=torch.int16, device=dev)
