@@ -168,3 +168,19 @@ def test_pack_validation(lib, args, expect):
 ])
 def test_gemm_packed_validation(lib, args, expect):
     assert lib.fp8_blockscaled_gemm_packed(*args) == expect
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/fp8bs.h compiles as C (no C++ in the ABI)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "fp8bs.h"\nint main(void) { return fp8bs_status_string(FP8BS_OK) == 0; }\n')
+    res = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                          "-I", cuda_inc, str(src)], capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
