@@ -78,6 +78,34 @@ WORKLOAD_TEXT = {
 # Algorithmic work per kernel launch (each operand read once, each output
 # written once; re-reads caused by tiling are not counted).
 # ---------------------------------------------------------------------------
+def step_launches(step, num_sms):
+    """Kernel launches of one step: one per kernel of the step, and the dense
+    GEMM's split-K reduction when it runs."""
+    n = len(step.kernels)
+    if step.kernels[-1] == "gemm":
+        n += gemm_kernel_launches(step.M, step.N, step.K, num_sms) - 1
+    return n
+
+
+def gemm_kernel_launches(M, N, K, num_sms):
+    """Kernels that one dense fp8_blockscaled_gemm call launches: the GEMM, and
+    the split-K reduction when the launcher cuts its last round of tiles.
+    Mirrors the launcher's rule: 256-column tiles on CTA pairs when the grid
+    fills the GPU (128 x 128 single-CTA tiles otherwise); tail = tiles %
+    resident clusters (one pair per two SMs); a split when 2 tail <= resident
+    and min(resident / tail, K / 512) >= 2."""
+    m_tiles = -(-M // 128)
+    if N % 256 == 0 and m_tiles * (N // 256) >= num_sms:
+        cg = 2 if m_tiles >= 2 else 1
+        tiles, resident = -(-m_tiles // cg) * (N // 256), num_sms // cg
+    else:
+        tiles, resident = m_tiles * (N // 128), num_sms
+    tail = tiles % resident
+    if tail == 0 or 2 * tail > resident:
+        return 1
+    return 2 if min(resident // tail, (K // 128) // 4) >= 2 else 1
+
+
 def requant_bytes(M, K):
     """FP8-cached activation -> 1x128 tiles of its transpose: the codes read
     and written once (1 B + 1 B per element) and one FP32 scale per 128
@@ -843,7 +871,8 @@ def run_ours(args):
             "tflops_gemm_only": flops / (per_kernel[step.kernels[-1]] * 1e-3) / 1e12,
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": len(step.kernels) * args.steps,
+            "gpu_launches": step_launches(step, torch.cuda.get_device_properties(device).multi_processor_count)
+                            * args.steps,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -27,3 +27,19 @@ def test_reference_arm_json_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_gemm_launch_count_mirrors_the_launcher():
+    """The launch count bench.py claims: the up-projection GEMM never splits
+    (42 tail tiles on 74 resident pairs), the down projection does (4 of
+    448), the decode and tiny shapes do not; 2048 x 2560 x 6144 splits (the
+    split-tail parity test's shape)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.gemm_kernel_launches(4096, 18432, 7168, 148) == 1
+    assert bench.gemm_kernel_launches(4096, 7168, 18432, 148) == 2
+    assert bench.gemm_kernel_launches(64, 18432, 7168, 148) == 1
+    assert bench.gemm_kernel_launches(128, 256, 256, 148) == 1
+    assert bench.gemm_kernel_launches(2048, 2560, 6144, 148) == 2
+    assert bench.gemm_kernel_launches(64, 7168, 18432, 148) == 2
