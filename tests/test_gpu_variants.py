@@ -42,11 +42,12 @@ def test_per_token(M, K):
     assert_scales_equal(f32(s), s_ref, "per-token scales")
 
 
-@pytest.mark.parametrize("M,K", [(1, 16), (130, 144), (300, 2048), (257, 528), (4096, 7168), (4097, 144),
-                                 (6000, 256)])
+@pytest.mark.parametrize("M,K", [(1, 16), (130, 144), (300, 2048), (257, 528), (2048, 144), (2049, 16),
+                                 (3000, 144), (2500, 1552), (4096, 64), (4096, 7168), (4097, 144), (6000, 256)])
 def test_per_channel(M, K):
-    """Up to 4096 rows: the one-pass cluster kernel (ragged rows and a ragged
-    last 64-channel block included); beyond: the two-pass kernels."""
+    """Up to 4096 rows: the one-pass cluster kernel, at every row count per
+    thread (ragged rows, a single and a ragged last 64-channel group
+    included); beyond: the two-pass kernels."""
     x = _edge_matrix(M, K, seed=3 * M + K)
     q, s = fb.fp8_quant_per_channel(x.to(DEV))
     torch.cuda.synchronize()
