@@ -39,7 +39,6 @@ import math
 import os
 import re
 import statistics
-import subprocess
 import sys
 import time
 
@@ -58,6 +57,9 @@ CSRC = os.path.join(ROOT, "fp8_fine_grained_14_b300", "csrc")
 # 4.5 PFLOP/s FP8 vs 2.25 PFLOP/s BF16).
 FP8_PER_BF16 = 2.0
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# Nominal (spec-sheet) B300 figures, reported beside the measured-peak
+# fractions: dense FP8 tensor rate and HBM3e bandwidth.
+NOMINAL = {"fp8_tflops": 4500.0, "hbm_gbs": 8000.0}
 
 WORKLOAD_TEXT = {
     "tiny": "tiny linear: X bf16 [128,256] ~N(0,1), W bf16 [256,256] ~N(0,0.02); "
@@ -177,59 +179,99 @@ def profiled_traffic(kernel, config):
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock and the clock event reasons of one GPU through
+    NVML (read-only queries) from a host thread, every `period_s` seconds or
+    as fast as NVML answers, while the host waits for the timed region.  A
+    10 ms region gets tens of samples (nvidia-smi's loop is 20 ms at best)."""
 
-    def __init__(self, device_index, period_ms=20):
-        self.proc = None
-        self.lines = []
+    REASONS = {"hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
+               "hw_thermal_slowdown": "nvmlClocksEventReasonHwThermalSlowdown",
+               "sw_thermal_slowdown": "nvmlClocksEventReasonSwThermalSlowdown",
+               "sw_power_cap": "nvmlClocksEventReasonSwPowerCap",
+               "hw_power_brake_slowdown": "nvmlClocksEventReasonHwPowerBrakeSlowdown"}
+
+    def __init__(self, device, period_s=0.0002):
+        import threading
+
+        self.samples = []  # (t, sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.error = None
+        self.period_s = period_s
+        self._stop = threading.Event()
+        self._thread = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            import pynvml
 
-    def warm(self):
-        """Wait (bounded) for the sampler's first line so the timed region is covered."""
-        if self.proc is None:
+            self.nv = pynvml
+            pynvml.nvmlInit()
+            self.handle = self._handle(device)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
+            self.bits = {k: getattr(pynvml, v, 0) for k, v in self.REASONS.items()}
+        except Exception as e:  # no NVML: report unsampled
+            self.error = f"{type(e).__name__}: {e}"
+            self.nv = None
+
+    def _handle(self, device):
+        nv = self.nv
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            return nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
+        except Exception:
+            return nv.nvmlDeviceGetHandleByIndex(device.index)
+
+    def _run(self):
+        nv, h = self.nv, self.handle
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+            except Exception as e:  # pragma: no cover
+                self.error = f"{type(e).__name__}: {e}"
+                return
+            self.samples.append((time.perf_counter(), float(mhz), int(reasons)))
+            if self.period_s:
+                time.sleep(self.period_s)
+
+    def start(self):
+        import threading
+
+        if self.nv is None:
             return
-        line = self.proc.stdout.readline()
-        if line:
-            self.first = line
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < 1.0:  # first sample before the region starts
+            time.sleep(0.0001)
 
     def stop(self):
-        if self.proc is None:
-            return
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        self.lines = [l for l in out.splitlines() if l.strip()]
-
-    def summary(self):
-        sms, maxes, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        if self.nv is not None:
             try:
-                sms.append(float(parts[1]))
-                maxes.append(float(parts[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sms:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
-                "samples": len(sms)}
+                self.nv.nvmlShutdown()
+            except Exception:
+                pass
+
+    def summary(self, t0=None, t1=None, ms=None):
+        """Samples between host times t0 and t1 (the timed region): median SM
+        MHz, the maximum SM clock, the reasons seen, and the region's time x
+        median MHz (cycles at the median clock)."""
+        sel = [s for s in self.samples if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0,
+                    "source": "nvml" if self.nv is not None else f"unavailable ({self.error})"}
+        seen = set()
+        for _, _, r in sel:
+            for name, bit in self.bits.items():
+                if bit and r & bit:
+                    seen.add(name)
+        med = statistics.median(m for _, m, _ in sel)
+        out = {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "sm_mhz_min": min(m for _, m, _ in sel),
+               "reasons": sorted(seen), "samples": len(sel), "source": "nvml, read-only, sampled in a host thread"}
+        if ms is not None:
+            out["region_ms_x_median_mhz"] = ms * med
+        return out
 
 
 # ---------------------------------------------------------------------------
@@ -306,8 +348,7 @@ class Step:
         self.sw = torch.empty((G * N // 128, K // 128), dtype=torch.float32, device=device)
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         self.offsets = inp["offsets"].to(device) if "offsets" in inp else None
-        self.kernels = ["act_quant"] + ([] if name == "decode" else ["weight_quant"]) + \
-            (["grouped_gemm"] if name == "grouped" else ["gemm"])
+        self.kernels = step_kernels(name)
         if name == "decode":
             with torch.cuda.stream(stream):
                 self.weight_quant()  # pre-quantised weights: outside the timed region
@@ -375,19 +416,21 @@ def time_device(step, stream, steps, warmup, dist, device):
     torch.cuda.synchronize(device)
     if step.fb.fp8bs_last_device_error(stream) != 0:
         raise RuntimeError("device status word set during warm-up")
-    sampler = ClockSampler(device.index)
-    sampler.warm()
+    sampler = ClockSampler(device)
+    sampler.start()
     barrier(dist, device)
     torch.cuda.synchronize(device)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     events = []
+    t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
             step.run(events)
         end.record(stream)
     torch.cuda.synchronize(device)
+    t1 = time.perf_counter()
     barrier(dist, device)
     sampler.stop()
     total_ms = start.elapsed_time(end)
@@ -401,7 +444,7 @@ def time_device(step, stream, steps, warmup, dist, device):
     status = step.fb.fp8bs_last_device_error(stream)
     if status != 0:
         raise RuntimeError(f"device status word {status} after the timed region")
-    return total_ms, per_kernel, sampler.summary()
+    return total_ms, per_kernel, sampler.summary(t0, t1, total_ms)
 
 
 def time_e2e(name, inp, step, stream, steps, warmup, device, fb):
@@ -450,12 +493,14 @@ def time_e2e(name, inp, step, stream, steps, warmup, device, fb):
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle timing (test infrastructure; only this leg of the benchmark
-# executes the oracle)
+# CPU oracle timing (test infrastructure; only these legs of the benchmark
+# execute the oracle).  The unchanged oracle runs row-parallel over every core
+# in this process's affinity mask (oracle.parallel: one worker process per
+# core, one BLAS thread each, row slices that the method keeps independent).
 # ---------------------------------------------------------------------------
 def oracle_threads():
-    """Threads the oracle's BLAS pool actually uses (its quantisation runs on
-    one thread)."""
+    """Threads the oracle's BLAS pool uses in this process (the per-row
+    timings of --rows run the oracle here, on one process)."""
     try:
         from threadpoolctl import threadpool_info
 
@@ -471,90 +516,116 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(name, inp, m_rows, n_rows):
-    """Run the oracle's whole path on rows [0, m_rows) of X and the first
-    n_rows (a multiple of 128) weight rows (of expert 0 when grouped).
-    Returns (seconds, FLOPs of the sample)."""
-    import oracle
-
-    x = inp["x"][:m_rows].float().numpy()
-    w = inp["w"][0] if name == "grouped" else inp["w"]
-    w = w[:n_rows].float().numpy()
-    K = x.shape[1]
-    t0 = time.perf_counter()
-    qa, sa = oracle.quant_act_1x128(x)
-    if name == "decode":
-        qw, sw = _decode_prequant_cache(w)
-    else:
-        qw, sw = oracle.quant_weight_128x128(w)
-    oracle.blockscaled_gemm(qa, sa, qw, sw)
-    return time.perf_counter() - t0, 2 * m_rows * n_rows * K
+def _bf16_bits(t):
+    return t.contiguous().view(torch.int16).numpy()
 
 
-_PREQ = {}
+class OracleSample:
+    """The oracle's whole step on rows [0, m_rows) of X and the first n_rows
+    (a multiple of 128) weight rows (of expert 0 when grouped), row-parallel
+    over the host's cores.  The weights of the decode workload are quantised
+    once, outside the timing, as the workload specifies."""
 
+    def __init__(self, pool, name, inp):
+        self.pool, self.name, self.inp = pool, name, inp
+        self._preq = {}
 
-def _decode_prequant_cache(w):
-    import oracle
+    def run(self, m_rows, n_rows):
+        x = _bf16_bits(self.inp["x"][:m_rows])
+        w = self.inp["w"][0] if self.name == "grouped" else self.inp["w"]
+        w = _bf16_bits(w[:n_rows])
+        K = x.shape[1]
+        if self.name == "decode" and n_rows not in self._preq:
+            self._preq[n_rows] = self.pool.quant_weight_128x128(w)
+        t0 = time.perf_counter()
+        qa, sa = self.pool.quant_act_1x128(x)
+        qw, sw = self._preq[n_rows] if self.name == "decode" else self.pool.quant_weight_128x128(w)
+        self.pool.blockscaled_gemm(qa, sa, qw, sw)
+        return time.perf_counter() - t0, 2 * m_rows * n_rows * K
 
-    key = (w.shape, float(w[0, 0]))
-    if key not in _PREQ:
-        _PREQ[key] = oracle.quant_weight_128x128(w)
-    return _PREQ[key]
+    def describe(self, m_rows, n_rows):
+        what = "expert 0's " if self.name == "grouped" else ""
+        quant = "quantisation of X" if self.name == "decode" else "quantisation of X and W"
+        return (f"CPU oracle (numpy; float64 GEMM) on X[:{m_rows}] and {what}W[:{n_rows}] with the full K: {quant} "
+                f"and the block-scaled GEMM, row-parallel over {self.pool.workers} worker processes (one per core "
+                f"of the {host_cores()} in this process's affinity mask, one BLAS thread each)")
 
 
 def cpu_baseline(name, inp, target_s=12.0):
+    from oracle.parallel import OraclePool
+
     M = inp["x"].shape[0]
     N = inp["w"].shape[-2]
-    m_rows = min(M, 512)
-    n_rows = min(N, 1024)
-    t, fl = oracle_sample(name, inp, m_rows, n_rows)
-    reps = max(1, min(20, int(target_s / max(t, 1e-3))))
-    tot_t, tot_f = t, fl
-    for _ in range(reps - 1):
-        t, fl = oracle_sample(name, inp, m_rows, n_rows)
-        tot_t += t
-        tot_f += fl
-    what = "expert 0's " if name == "grouped" else ""
-    return {
-        "value": tot_f / tot_t / 1e12,
-        "unit": "TFLOP/s",
-        "cores": oracle_threads(),
-        "kind": "oracle",
-        "sample": (f"CPU oracle (numpy, float64 GEMM through BLAS) on X[:{m_rows}] and {what}W[:{n_rows}] with the "
-                   f"full K, quantisation{' of X' if name == 'decode' else ''} and GEMM, {reps} repetitions "
-                   f"({tot_t:.1f} s); value = sample FLOPs / sample time; quantisation on 1 thread, BLAS on "
-                   f"{oracle_threads()} of the {host_cores()} cores in this process's affinity mask"),
-    }
+    m_rows = min(M, 1024)
+    n_rows = min(N, 2048)
+    with OraclePool() as pool:
+        smp = OracleSample(pool, name, inp)
+        smp.run(min(M, 128), min(N, 128))  # warm the workers
+        t, fl = smp.run(m_rows, n_rows)
+        reps = max(1, min(20, int(target_s / max(t, 1e-3))))
+        tot_t, tot_f = t, fl
+        for _ in range(reps - 1):
+            t, fl = smp.run(m_rows, n_rows)
+            tot_t += t
+            tot_f += fl
+        return {
+            "value": tot_f / tot_t / 1e12,
+            "unit": "TFLOP/s",
+            "cores": pool.workers,
+            "kind": "oracle",
+            "sample": f"{smp.describe(m_rows, n_rows)}; {reps} repetitions ({tot_t:.1f} s); value = sample FLOPs / "
+                      f"sample time",
+        }
+
+
+def arm_config(name, M, N, K, G, kernels, world):
+    """The `config` of the JSON line, identical for both arms."""
+    return {"workload": WORKLOAD_TEXT[name], "name": name, "M": M, "N": N, "K": K, "G": G,
+            "step": " + ".join(kernels), "l2": "no flush: inputs larger than L2 (step working set > 126 MB)",
+            "parallelism": f"replicas x{world}"}
+
+
+def step_kernels(name):
+    """The kernels of one step, in order: the weights are quantised (once per
+    weight update; the decode workload's weights are pre-quantised), then the
+    activations online, then the GEMM."""
+    return ([] if name == "decode" else ["weight_quant"]) + ["act_quant"] + \
+        (["grouped_gemm"] if name == "grouped" else ["gemm"])
 
 
 # ---------------------------------------------------------------------------
 # Arms
 # ---------------------------------------------------------------------------
 def run_reference(args):
+    from oracle.parallel import OraclePool
+
     rank, world, _ = dist_env()
     if rank != 0:
         return
     name = args.config
     inp = make_inputs(name, seed=0)
-    M = inp["x"].shape[0]
-    N = inp["w"].shape[-2]
+    s = shapes(name, inp)
+    M, N, K, G = s["M"], s["N"], s["K"], s["G"]
     # size each step's sample so that warm-up + steps end within ~150 s
     budget = 150.0 / max(1, args.steps + args.warmup)
-    n_rows = min(N, 128)
-    m_rows = min(M, 8)
-    t, _ = oracle_sample(name, inp, m_rows, n_rows)
-    while m_rows * 2 <= min(M, 512) and t * 2 <= budget:
-        m_rows *= 2
-        t, _ = oracle_sample(name, inp, m_rows, n_rows)
-    for _ in range(args.warmup):
-        oracle_sample(name, inp, m_rows, n_rows)
-    t0 = time.perf_counter()
-    flops = 0
-    for _ in range(args.steps):
-        _, fl = oracle_sample(name, inp, m_rows, n_rows)
-        flops += fl
-    elapsed = time.perf_counter() - t0
+    with OraclePool() as pool:
+        smp = OracleSample(pool, name, inp)
+        n_rows = min(N, 512)
+        m_rows = min(M, 16)
+        t, _ = smp.run(m_rows, n_rows)
+        while m_rows * 2 <= min(M, 2048) and t * 2 <= budget:
+            m_rows *= 2
+            t, _ = smp.run(m_rows, n_rows)
+        for _ in range(args.warmup):
+            smp.run(m_rows, n_rows)
+        t0 = time.perf_counter()
+        flops = 0
+        for _ in range(args.steps):
+            _, fl = smp.run(m_rows, n_rows)
+            flops += fl
+        elapsed = time.perf_counter() - t0
+        cores = pool.workers
+        sample = smp.describe(m_rows, n_rows)
     value = flops / elapsed / 1e12
     unit = "TFLOP/s"
     line = {
@@ -563,11 +634,9 @@ def run_reference(args):
         "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[name], "M": M, "N": N, "K": inp["x"].shape[1],
-                   "parallelism": "rank 0 only (CPU)"},
-        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle_threads(), "kind": "oracle",
-                         "sample": f"per step: CPU oracle quantisation + GEMM on X[:{m_rows}] and W[:{n_rows}] "
-                                   f"with the full K; value = sample FLOPs / time"},
+        "config": arm_config(name, M, N, K, G, step_kernels(name), args.gpus),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {sample}; rank 0 only; value = sample FLOPs / time"},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -842,6 +911,11 @@ def run_ours(args):
         sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
         roofline["peak_sustained"] = sustained
         roofline["frac_of_sustained"] = d["achieved"] / sustained
+    nominal = NOMINAL["fp8_tflops"] if d["bound"] == "tensor" else NOMINAL["hbm_gbs"]
+    roofline["peak_nominal"] = nominal
+    roofline["frac_of_nominal"] = d["achieved"] / nominal
+    for k, v in kern.items():
+        v["frac_of_nominal"] = v["achieved"] / (NOMINAL["fp8_tflops"] if v["bound"] == "tensor" else NOMINAL["hbm_gbs"])
 
     e2e = None
     if not args.no_e2e:
@@ -862,9 +936,7 @@ def run_ours(args):
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 (f32 accumulate, bf16 out)", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[name], "name": name, "M": M, "N": N, "K": K, "G": step.G,
-                       "step": " + ".join(step.kernels), "l2": "no flush: inputs larger than L2 "
-                       "(step working set > 126 MB)", "parallelism": f"replicas x{world}"},
+            "config": arm_config(name, M, N, K, step.G, step.kernels, world),
             "roofline": roofline,
             "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for k, v in kern.items()},

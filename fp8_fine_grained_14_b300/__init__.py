@@ -13,6 +13,7 @@ _API = (
     "fp8_quant_weight_128x128",
     "fp8_blockscaled_gemm",
     "fp8_blockscaled_gemm_noalloc",
+    "fp8_blockscaled_gemm_workspace_bytes",
     "fp8_blockscaled_gemm_residual",
     "fp8_blockscaled_grouped_gemm",
     "fp8_dequant_weight_128x128",

@@ -50,6 +50,7 @@ EXPORTS = {
     "fp8_blockscaled_gemm_rowscaled": [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64, _p],
     "fp8_blockscaled_gemm_rowscaled_f32": [_p, _i64, _p, _i64, _p, _i64, _p, _i64, _p, _i64, _i64, _i64, _i64,
                                            _p],
+    "fp8_blockscaled_gemm_workspace_bytes": [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)],
     "fp8bs_status_string": [ctypes.c_int],
     "fp8bs_last_error_detail": [],
     "fp8bs_last_device_error": [_p],
@@ -209,11 +210,21 @@ def fp8_blockscaled_gemm_residual(qa, sa, qw, sw, residual, y=None, stream=None)
     return y
 
 
+def fp8_blockscaled_gemm_workspace_bytes(M, N, K):
+    """Bytes of split-K workspace that fp8_blockscaled_gemm takes from the
+    library's pool for an M x N x K product on the current device (0: the
+    shape's tiles are not split)."""
+    out = ctypes.c_size_t(0)
+    _check("fp8_blockscaled_gemm_workspace_bytes", lib.fp8_blockscaled_gemm_workspace_bytes(M, N, K, ctypes.byref(out)))
+    return out.value
+
+
 def fp8_blockscaled_gemm_noalloc(qa, sa, qw, sw, y=None, stream=None):
-    """fp8_blockscaled_gemm (BF16 out) with the split-K workspace in the
-    library's fixed static device array instead of its memory pool: the call
-    allocates nothing.  Calls that split share that array, so keep them on
-    one stream."""
+    """fp8_blockscaled_gemm (BF16 out) for callers that cannot allocate device
+    memory: the split-K workspace lives in the library's fixed static device
+    array instead of its memory pool, so the C call allocates nothing (this
+    wrapper allocates y only when it is not given).  Calls share that array,
+    so calls that could overlap on the GPU must be ordered (one stream)."""
     _require(qa, torch.uint8, "qa", 2)
     _require(qw, torch.uint8, "qw", 2)
     _require(sa, torch.float32, "sa", 2)

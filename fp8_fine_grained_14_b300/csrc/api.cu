@@ -21,10 +21,13 @@ namespace fp8bs {
 // variable).  Kernels record failures here; fp8bs_last_device_error reads it.
 __device__ unsigned g_status_word;
 
-// Fixed split-K workspace of fp8_blockscaled_gemm_noalloc, one per device:
-// 20 MiB covers the largest split tail on a 148-SM device (a split tail has
-// at most one work unit per resident cluster, each unit 128 rows x 256
-// columns of FP32 per CTA).
+// Fixed split-K workspace of fp8_blockscaled_gemm_noalloc, one per device
+// (every device that loads the library holds it until the process exits).
+// 20 MiB covers the largest split tail of a device with up to 160 SMs: a
+// split tail has at most one work unit per resident cluster, each unit 128
+// rows x 256 columns of FP32 per CTA, i.e. 128 KiB per SM.  Nothing in it
+// needs to start at zero: each unit writes its whole partial before the
+// reduction kernel reads it.
 constexpr size_t kGemmScratchBytes = size_t(20) << 20;
 static __device__ __align__(256) unsigned char g_gemm_scratch[kGemmScratchBytes];
 
@@ -39,6 +42,14 @@ struct DeviceSlot {
   std::once_flag once;
   DeviceInfo info;
   cudaError_t err = cudaSuccess;
+  // the GEMM workspace pool, created at the first split tail that needs it
+  std::once_flag pool_once;
+  cudaMemPool_t pool = nullptr;
+  // this device's address of g_gemm_scratch, looked up at the first
+  // fp8_blockscaled_gemm_noalloc call on the device
+  std::once_flag scratch_once;
+  float* scratch = nullptr;
+  cudaError_t scratch_err = cudaSuccess;
 };
 DeviceSlot g_devices[kMaxDevices];
 
@@ -86,21 +97,6 @@ const DeviceInfo* current_device_info(cudaError_t* err) {
     slot.info.status = static_cast<unsigned*>(addr);
     const unsigned zero = 0;
     if (slot.err == cudaSuccess) slot.err = cudaMemcpy(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice);
-    slot.info.workspace_pool = nullptr;
-    if (slot.err == cudaSuccess) {
-      cudaMemPoolProps props = {};
-      props.allocType = cudaMemAllocationTypePinned;
-      props.location.type = cudaMemLocationTypeDevice;
-      props.location.id = dev;
-      cudaMemPool_t pool = nullptr;
-      if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
-        cuuint64_t keep = ~static_cast<cuuint64_t>(0);
-        (void)cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-        slot.info.workspace_pool = pool;
-      } else {
-        (void)cudaGetLastError();  // no pool: GEMM tails run unsplit
-      }
-    }
   });
   if (slot.err != cudaSuccess) {
     *err = slot.err;
@@ -108,6 +104,38 @@ const DeviceInfo* current_device_info(cudaError_t* err) {
   }
   *err = cudaSuccess;
   return &slot.info;
+}
+
+cudaMemPool_t gemm_workspace_pool(const DeviceInfo& dev) {
+  DeviceSlot& slot = g_devices[dev.ordinal];
+  std::call_once(slot.pool_once, [&slot, &dev]() {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev.ordinal;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+      cuuint64_t keep = ~static_cast<cuuint64_t>(0);
+      (void)cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      slot.pool = pool;
+    } else {
+      (void)cudaGetLastError();  // no pool: GEMM tails run unsplit
+    }
+  });
+  return slot.pool;
+}
+
+// Device address of this device's g_gemm_scratch (the host-side name is only
+// a stand-in), looked up once per device with that device current.
+float* gemm_scratch_address(const DeviceInfo& dev, cudaError_t* err) {
+  DeviceSlot& slot = g_devices[dev.ordinal];
+  std::call_once(slot.scratch_once, [&slot]() {
+    void* addr = nullptr;
+    slot.scratch_err = cudaGetSymbolAddress(&addr, g_gemm_scratch);
+    slot.scratch = slot.scratch_err == cudaSuccess ? static_cast<float*>(addr) : nullptr;
+  });
+  *err = slot.scratch_err;
+  return slot.scratch;
 }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
@@ -230,22 +258,22 @@ fp8bs_status dense_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t l
   cudaError_t e;
   const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
   if (dev == nullptr) return cuda_failure("device query", e);
-  float* scratch = nullptr;
-  size_t scratch_bytes = 0;
+  fp8bs::Workspace ws;
   if (use_static_scratch) {
-    void* addr = nullptr;
-    e = cudaGetSymbolAddress(&addr, fp8bs::g_gemm_scratch);  // this device's copy
-    if (e != cudaSuccess) return cuda_failure("scratch address", e);
-    scratch = static_cast<float*>(addr);
-    scratch_bytes = fp8bs::kGemmScratchBytes;
+    ws.scratch = fp8bs::gemm_scratch_address(*dev, &e);
+    if (ws.scratch == nullptr) return cuda_failure("scratch address", e);
+    ws.scratch_bytes = fp8bs::kGemmScratchBytes;
   }
   e = fp8bs::launch_blockscaled_gemm(*dev, qa, ldqa, sa, ld_sa, qw, ldqw, sw, y, ldy, out_bytes == 4, M, N, K,
-                                     stream, scratch, scratch_bytes, res, ldr);
-  if (e == cudaErrorMemoryAllocation && use_static_scratch) {
-    std::snprintf(fp8bs::t_detail, sizeof(fp8bs::t_detail), "%s: split-K workspace larger than the static scratch", name);
+                                     stream, &ws, res, ldr);
+  if (e != cudaSuccess) return cuda_failure(name, e);
+  if (ws.too_small) {
+    std::snprintf(fp8bs::t_detail, sizeof(fp8bs::t_detail),
+                  "%s: the split-K tail needs %zu bytes of workspace, more than the %zu-byte static scratch", name,
+                  ws.needed, ws.scratch_bytes);
     return FP8BS_ERR_UNSUPPORTED_SHAPE;
   }
-  return e == cudaSuccess ? FP8BS_OK : cuda_failure(name, e);
+  return FP8BS_OK;
 }
 
 fp8bs_status grouped_gemm(int32_t G, const int32_t* group_offsets_dev, int64_t M_total, const void* qa, int64_t ldqa,
@@ -501,6 +529,24 @@ fp8bs_status fp8_blockscaled_gemm_noalloc(const void* qa, int64_t ldqa, const fl
                                           int64_t K, cudaStream_t stream) {
   return dense_gemm(qa, ldqa, sa, ld_sa, qw, ldqw, sw, y_bf16, ldy, 2, M, N, K, stream,
                     "fp8_blockscaled_gemm_noalloc launch", true);
+}
+
+fp8bs_status fp8_blockscaled_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+  if (bytes == nullptr || M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (K == 0 || K % 128 != 0 || N == 0 || N % 128 != 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return FP8BS_OK;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  fp8bs::Workspace ws;
+  ws.plan_only = true;
+  e = fp8bs::launch_blockscaled_gemm(*dev, nullptr, K, nullptr, M, nullptr, K, nullptr, nullptr, N, false, M, N, K,
+                                     nullptr, &ws);
+  if (e != cudaSuccess) return cuda_failure("fp8_blockscaled_gemm_workspace_bytes", e);
+  *bytes = ws.needed;
+  return FP8BS_OK;
 }
 
 fp8bs_status fp8_blockscaled_gemm_f32(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa, const void* qw,

@@ -757,21 +757,19 @@ int max_resident_clusters(const DeviceInfo& dev, const cudaLaunchConfig_t& cfg) 
   return n;
 }
 
-// Persistent launch: one cluster of CG CTAs per CG SMs, at most one per
-// cluster tile.
 // Smallest K slice of a split tail tile, in 128-K chunks.
 constexpr int kMinSplitChunks = 4;
 
 // Persistent launch: one cluster of CG CTAs per CG SMs, at most one per work
-// item.  When the dense tiles leave a last round (or a single round) that fills
-// at most half of the resident clusters, those tiles are split along K over the idle
-// clusters (FP32 partials in a workspace: `scratch` when given, else
-// stream-ordered memory from the library's per-device pool) and summed by
-// split_tail_reduce_kernel.
+// item.  When the dense tiles leave a last round (or a single round) that
+// fills at most half of the resident clusters, those tiles are split along K
+// over the idle clusters (FP32 partials in a workspace, see Workspace) and
+// summed by split_tail_reduce_kernel.  A split tail has at most one unit per
+// resident cluster, so the workspace never exceeds BM x BN FP32 values per SM.
 template <int BN, int STAGES, bool GROUPED, int CG, bool F32, bool RS, bool HALF_A = false, bool RES = false>
 cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                           const CUtensorMap& tmY, const Params& p0, int64_t cluster_tiles, cudaStream_t stream,
-                          float* scratch, size_t scratch_bytes) {
+                          Workspace* ws) {
   using L = Smem<BN, STAGES, CG, RS, HALF_A>;
   auto kernel = blockscaled_gemm_kernel<BN, STAGES, GROUPED, CG, F32, RS, HALF_A, RES>;
   if (BN == 256) {
@@ -802,35 +800,47 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   p.t_full = static_cast<int32_t>(cluster_tiles);
   p.split = 1;
   p.ws = nullptr;
-  bool owned = false;
+  int64_t tail = 0, split = 1;
+  size_t bytes = 0;
   if constexpr (!GROUPED) {
     // the last round's tiles (all of them when the grid fills at most half of
     // the resident clusters, e.g. skinny products with few column tiles)
-    const int64_t tail = cluster_tiles % resident;
+    tail = cluster_tiles % resident;
     if (tail > 0 && 2 * tail <= resident) {
-      int64_t split = resident / tail;
+      split = resident / tail;
       if (split > p.KB / kMinSplitChunks) split = p.KB / kMinSplitChunks;
-      const size_t bytes = static_cast<size_t>(tail * split) * CG * BM * BN * sizeof(float);
-      float* ws = nullptr;
-      if (split >= 2) {
-        if (scratch != nullptr) {
-          if (bytes > scratch_bytes) return cudaErrorMemoryAllocation;
-          ws = scratch;
-        } else if (dev.workspace_pool != nullptr &&
-                   cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), bytes, dev.workspace_pool, stream) ==
-                       cudaSuccess) {
-          owned = true;
-        } else {
-          (void)cudaGetLastError();  // no workspace: run the tail tiles whole
-          ws = nullptr;
-        }
+      if (split < 2) split = 1;
+      bytes = split > 1 ? static_cast<size_t>(tail * split) * CG * BM * BN * sizeof(float) : 0;
+    }
+  }
+  if (ws != nullptr) {
+    ws->needed = bytes;
+    if (ws->plan_only) return cudaSuccess;
+    if (ws->scratch != nullptr && bytes > ws->scratch_bytes) {
+      ws->too_small = true;
+      return cudaSuccess;
+    }
+  }
+  bool owned = false;
+  if (bytes > 0) {
+    float* buf = nullptr;
+    if (ws != nullptr && ws->scratch != nullptr) {
+      buf = ws->scratch;
+    } else {
+      cudaMemPool_t pool = gemm_workspace_pool(dev);
+      if (pool != nullptr &&
+          cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), bytes, pool, stream) == cudaSuccess) {
+        owned = true;
+      } else {
+        (void)cudaGetLastError();  // no workspace: run the tail tiles whole
+        buf = nullptr;
       }
-      if (ws != nullptr) {
-        p.ws = ws;
-        p.split = static_cast<int32_t>(split);
-        p.t_full = static_cast<int32_t>(cluster_tiles - tail);
-        p.n_items = static_cast<int32_t>(p.t_full + tail * split);
-      }
+    }
+    if (buf != nullptr) {
+      p.ws = buf;
+      p.split = static_cast<int32_t>(split);
+      p.t_full = static_cast<int32_t>(cluster_tiles - tail);
+      p.n_items = static_cast<int32_t>(p.t_full + tail * split);
     }
   }
   const int64_t clusters = p.n_items < resident ? p.n_items : resident;
@@ -899,22 +909,22 @@ enum class Shape { kNarrow, kNarrowHalfA, kWide, kPair };
 template <bool GROUPED, bool F32, bool RS = false, bool RES = false>
 cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmY, const Params& p, int64_t cluster_tiles, cudaStream_t stream,
-                         float* scratch = nullptr, size_t scratch_bytes = 0) {
+                         Workspace* ws = nullptr) {
   switch (shape) {
     case Shape::kNarrow:
       return launch_kernel<128, RS ? kStages128RS : kStages128, GROUPED, 1, F32, RS, false, RES>(
-          dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
+          dev, tmA, tmB, tmY, p, cluster_tiles, stream, ws);
     case Shape::kNarrowHalfA:
       if constexpr (!GROUPED && !RS)
-        return launch_kernel<128, kStages128HalfA, false, 1, F32, false, true, RES>(dev, tmA, tmB, tmY, p, cluster_tiles,
-                                                                             stream, scratch, scratch_bytes);
+        return launch_kernel<128, kStages128HalfA, false, 1, F32, false, true, RES>(dev, tmA, tmB, tmY, p,
+                                                                                   cluster_tiles, stream, ws);
       return cudaErrorInvalidValue;
     case Shape::kWide:
       return launch_kernel<256, RS ? kStages256RS : kStages256, GROUPED, 1, F32, RS, false, RES>(
-          dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
+          dev, tmA, tmB, tmY, p, cluster_tiles, stream, ws);
     case Shape::kPair:
       return launch_kernel<256, RS ? kStagesPairRS : kStagesPair, GROUPED, 2, F32, RS, false, RES>(
-          dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes);
+          dev, tmA, tmB, tmY, p, cluster_tiles, stream, ws);
   }
   return cudaErrorInvalidValue;
 }
@@ -924,7 +934,7 @@ cudaError_t launch_shape(Shape shape, const DeviceInfo& dev, const CUtensorMap& 
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
                                     int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                                    float* scratch, size_t scratch_bytes, const void* res, int64_t ldr) {
+                                    Workspace* ws, const void* res, int64_t ldr) {
   // Wide tiles (BN = 256) halve the operand traffic per FLOP; narrow ones keep
   // every SM busy when there are few tiles (skinny, decode-shaped M).
   const int64_t m_tiles = (M + BM - 1) / BM;
@@ -935,11 +945,13 @@ cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64
   const int BN = wide ? 256 : 128;
   const int out_bytes = y_f32 ? 4 : 2;
   const uint32_t a_rows = shape == Shape::kNarrowHalfA ? BM / 2 : BM;
-  CUtensorMap tmA, tmB, tmY;
-  if (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, BK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, N, ldqw, BK, BN / CG, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tmY, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M,
-                    ldy * out_bytes, kEpiRowBytes / out_bytes, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+  CUtensorMap tmA = {}, tmB = {}, tmY = {};
+  const bool plan_only = ws != nullptr && ws->plan_only;  // the maps are not needed to plan
+  if (!plan_only &&
+      (!make_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, ldqa, BK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+       !make_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qw, K, N, ldqw, BK, BN / CG, CU_TENSOR_MAP_SWIZZLE_128B) ||
+       !make_tmap_2d(&tmY, y_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, y, N, M,
+                     ldy * out_bytes, kEpiRowBytes / out_bytes, 32, CU_TENSOR_MAP_SWIZZLE_128B)))
     return cudaErrorInvalidValue;
   Params p = make_params(dev, sa, ld_sa, sw, y, ldy, M, N, K, nullptr, 1);
   p.res = static_cast<const uint16_t*>(res);
@@ -949,12 +961,10 @@ cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64
     // the residual epilogue is its own kernel variant (BF16 output only), so
     // the plain GEMM keeps its register budget
     if (y_f32) return cudaErrorInvalidValue;
-    return launch_shape<false, false, false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch,
-                                                   scratch_bytes);
+    return launch_shape<false, false, false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, ws);
   }
-  return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch, scratch_bytes)
-               : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, scratch,
-                                            scratch_bytes);
+  return y_f32 ? launch_shape<false, true>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, ws)
+               : launch_shape<false, false>(shape, dev, tmA, tmB, tmY, p, cluster_tiles, stream, ws);
 }
 
 cudaError_t launch_blockscaled_gemm_packed(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,

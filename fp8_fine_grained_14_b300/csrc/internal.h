@@ -13,15 +13,26 @@ struct DeviceInfo {
   int num_sms;
   int max_smem_optin;
   unsigned* status;  // device address of this device's status word
-  // Library-owned stream-ordered memory pool for GEMM workspaces (split-K
-  // partials).  It keeps freed memory for reuse instead of returning it at
-  // every synchronisation; null when the device offers no memory pools.
-  cudaMemPool_t workspace_pool;
 };
 
 // Per-device facts, looked up once per device (thread-safe).  Returns nullptr
 // and sets *err when the device cannot be queried.
 const DeviceInfo* current_device_info(cudaError_t* err);
+
+// Library-owned stream-ordered memory pool of a device for GEMM split-K
+// workspaces, created on first use (thread-safe).  It keeps freed memory for
+// reuse instead of returning it at every synchronisation.  Null when the
+// device offers no memory pools (split tails then run unsplit).
+cudaMemPool_t gemm_workspace_pool(const DeviceInfo& dev);
+
+// Where the FP32 partials of a split-K tail go (see launch_blockscaled_gemm).
+struct Workspace {
+  float* scratch = nullptr;   // a fixed device region; null: the device's workspace pool
+  size_t scratch_bytes = 0;   // its size
+  bool plan_only = false;     // decide the tile plan and report `needed`; launch nothing
+  size_t needed = 0;          // out: workspace bytes the split tail needs (0: no split)
+  bool too_small = false;     // out: scratch given and smaller than `needed` (nothing launched)
+};
 
 uint64_t wait_timeout_ns();
 
@@ -38,16 +49,18 @@ cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, in
 // Returns cudaErrorInvalidValue when a tensor map cannot be encoded.
 // y is BF16 (y_f32 false) or FP32 (y_f32 true); ldy in elements of that type.
 // When the last round of tiles would leave most SMs idle, the tail tiles are
-// split along K; their FP32 partials go to `scratch` (scratch_bytes long; the
-// launch fails with cudaErrorMemoryAllocation if it is too small) or, when scratch
-// is null, to stream-ordered memory from DeviceInfo::workspace_pool.  res (BF16,
-// row stride ldr elements), when not null, is added to the FP32 result before
-// the output rounding; it may be y itself (same stride) for an in-place update.
+// split along K; their FP32 partials go to ws->scratch, or, when that is null,
+// to stream-ordered memory from gemm_workspace_pool (allocated and freed on
+// `stream` around the two kernels).  ws->needed reports the bytes; with a
+// scratch region smaller than that, nothing is launched and ws->too_small is
+// set.  With ws->plan_only only ws->needed is computed.  ws may be null (the
+// pool).  res (BF16, row stride ldr elements), when not null, is added to the
+// FP32 result before the output rounding; it may be y itself (same stride)
+// for an in-place update.
 cudaError_t launch_blockscaled_gemm(const DeviceInfo& dev, const void* qa, int64_t ldqa, const float* sa,
                                     int64_t ld_sa, const void* qw, int64_t ldqw, const float* sw, void* y,
                                     int64_t ldy, bool y_f32, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-                                    float* scratch = nullptr, size_t scratch_bytes = 0, const void* res = nullptr,
-                                    int64_t ldr = 0);
+                                    Workspace* ws = nullptr, const void* res = nullptr, int64_t ldr = 0);
 
 // As launch_blockscaled_gemm with B as packed 128x128 tiles wp[N/128][K/128]
 // (fp8_pack_weight_128x128's layout); single-CTA tile shapes only.

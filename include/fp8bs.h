@@ -22,6 +22,18 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or retains them.  Base pointers must be 16-byte
  *     aligned (FP8BS_ERR_MISALIGNED otherwise).
+ *   - Memory the library owns: per device, one status word (a __device__
+ *     variable) and the fixed 20 MiB static scratch array of
+ *     fp8_blockscaled_gemm_noalloc (both part of the loaded module), and one
+ *     stream-ordered memory pool for the split-K workspace of
+ *     fp8_blockscaled_gemm, _f32 and _residual.  The pool is created by the
+ *     first of those calls whose last round of tiles is split; each such call
+ *     takes at most 128 KiB per SM of the device (18.5 MiB on 148 SMs) from it
+ *     on its stream and returns it on the same stream after the two kernels.
+ *     The pool keeps freed memory for reuse (it is never trimmed while the
+ *     process runs), so repeated calls do not allocate from the device again.
+ *     fp8_blockscaled_gemm_workspace_bytes tells how much a shape takes.
+ *     Nothing else is allocated.
  *   - Matrices are row-major; "ld" arguments are row strides in ELEMENTS.
  *     BF16 and FP8 row strides must make 16-byte multiples (ld % 8 == 0 for
  *     BF16, ld % 16 == 0 for FP8 codes).
@@ -45,6 +57,7 @@
 #ifndef FP8BS_H
 #define FP8BS_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -93,6 +106,13 @@ fp8bs_status fp8_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, 
  * Chunk products accumulate in FP32 tensor memory; each chunk is scaled and
  * added to an FP32 register accumulator; the result is rounded to BF16
  * (round to nearest even).
+ * Workspace: when the last round of output tiles would leave at least half
+ * of the SMs idle, those tiles are split along K over the idle SMs, and their
+ * FP32 partial sums go to a workspace drawn from the library's per-device
+ * pool on `stream` (at most 128 KiB per SM; see the conventions above and
+ * fp8_blockscaled_gemm_workspace_bytes).  A second kernel sums the slices in
+ * a fixed order, so results do not depend on timing.  Without a pool on the
+ * device the tail runs unsplit (same results).
  */
 fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
                                   const void* qw, int64_t ldqw, const float* sw,
@@ -103,6 +123,7 @@ fp8bs_status fp8_blockscaled_gemm(const void* qa, int64_t ldqa, const float* sa,
  * As fp8_blockscaled_gemm, with FP32 output (paragraph 4: the FP8 GEMMs
  * "produce outputs in BF16 or FP32"): y[m, n] is the FP32 accumulator itself,
  * not rounded further.  y : [M, N] FP32, row stride ldy (elements, ldy % 4 == 0).
+ * Split-K workspace from the library's pool as for fp8_blockscaled_gemm.
  */
 fp8bs_status fp8_blockscaled_gemm_f32(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
                                       const void* qw, int64_t ldqw, const float* sw,
@@ -308,7 +329,8 @@ fp8bs_status fp8_swiglu_quant_act_1x128(const void* gate_up_bf16, int64_t M, int
  * outputs; the addition fuses the block's residual stream into the
  * epilogue).  R and Y are either the same buffer with the same stride (an
  * in-place update of the residual stream) or disjoint.  R must be 16-byte
- * aligned with ldr % 8 == 0 and ldr >= N; otherwise as fp8_blockscaled_gemm.
+ * aligned with ldr % 8 == 0 and ldr >= N; otherwise as fp8_blockscaled_gemm,
+ * split-K workspace from the library's pool included.
  */
 fp8bs_status fp8_blockscaled_gemm_residual(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
                                            const void* qw, int64_t ldqw, const float* sw,
@@ -316,21 +338,47 @@ fp8bs_status fp8_blockscaled_gemm_residual(const void* qa, int64_t ldqa, const f
                                            int64_t M, int64_t N, int64_t K, cudaStream_t stream);
 
 /*
- * fp8_blockscaled_gemm without any allocation.  The pages have no counterpart
- * of this call: it exists for callers that must not allocate (e.g. inside
- * graph capture with allocation disabled).  Same arguments, layouts, results
- * (bit for bit) and error behaviour as fp8_blockscaled_gemm, except that when
- * the last round of tiles is split along K, the FP32 partials go to a fixed
- * 20 MiB static device array of the library (one per device) instead of the
- * library's stream-ordered pool.  That array is shared by every call on the
- * device, so calls whose tails split must be ordered (one stream, or
- * synchronised).  Returns FP8BS_ERR_UNSUPPORTED_SHAPE if a problem's split
- * tail would need more than the array holds (not reachable on 148-SM parts).
+ * fp8_blockscaled_gemm for callers that cannot allocate device memory.  The
+ * pages have no counterpart of this call; it serves code that runs where a
+ * cudaMalloc or a memory-pool allocation is not allowed or not safe: a host
+ * whose device memory is all handed out by another allocator (a framework,
+ * or a fixed arena planned ahead of time), code that must not add the
+ * implicit synchronisation or the latency of an allocation to its step, or
+ * code that must not fail for lack of memory half-way through a step.
+ *
+ * Arguments, layouts, results (bit for bit) and errors are those of
+ * fp8_blockscaled_gemm, except for the workspace of a split-K tail: its FP32
+ * partials go to a fixed static device array of 20 MiB in the library (one
+ * per device, part of the loaded module, held until the process exits)
+ * instead of the pool.  The call makes no cudaMalloc, cudaFree or pool
+ * allocation and creates no pool.  Nothing in the array needs clearing
+ * between calls (every partial is written before it is read).
+ *   - A shape whose split tail would need more than 20 MiB returns
+ *     FP8BS_ERR_UNSUPPORTED_SHAPE and launches nothing
+ *     (fp8_blockscaled_gemm_workspace_bytes tells the need; devices with up
+ *     to 160 SMs never need more).
+ *   - Every call on a device shares the array: calls whose work overlaps on
+ *     the GPU (different streams without ordering between them) race on it
+ *     and may return wrong results.  Order them on one stream, or with events.
+ *   - The first call on a device, like the first call of any entry point,
+ *     sets up per-device state with synchronous runtime calls (device
+ *     attributes, the addresses of the library's device variables, clearing
+ *     the status word).  Make that first call before any stream capture.
  */
 fp8bs_status fp8_blockscaled_gemm_noalloc(const void* qa, int64_t ldqa, const float* sa, int64_t ld_sa,
                                           const void* qw, int64_t ldqw, const float* sw,
                                           void* y_bf16, int64_t ldy,
                                           int64_t M, int64_t N, int64_t K, cudaStream_t stream);
+
+/*
+ * Split-K workspace, in bytes, that fp8_blockscaled_gemm takes from the
+ * library's pool for an M x N x K product on the current device (and that
+ * fp8_blockscaled_gemm_noalloc needs in its static array): 0 when the shape's
+ * tiles are not split.  No counterpart in the pages.  Nothing is launched or
+ * allocated.  Shape errors as for fp8_blockscaled_gemm; null `bytes`
+ * returns FP8BS_ERR_INVALID_ARG.
+ */
+fp8bs_status fp8_blockscaled_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 /*
  * Text naming the CUDA error (and the step) behind the last FP8BS_ERR_CUDA

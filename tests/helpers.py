@@ -45,6 +45,24 @@ def assert_gemm_close(y_gpu, y_ref, rms=None, what="gemm"):
             f"rms={rms:.4g}")
 
 
+def assert_gemm_close_rows(y_gpu, y_ref, rows_per_chunk=4096, what="gemm"):
+    """assert_gemm_close over a large output, in row chunks (bounded host
+    memory), with rms taken over the WHOLE reference output."""
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    assert tuple(y_gpu.shape) == y_ref.shape, (tuple(y_gpu.shape), y_ref.shape)
+    rms = float(np.sqrt(np.mean(np.square(y_ref)))) if y_ref.size else 0.0
+    for r0 in range(0, y_ref.shape[0], rows_per_chunk):
+        r1 = min(y_ref.shape[0], r0 + rows_per_chunk)
+        assert_gemm_close(f32(y_gpu[r0:r1]), y_ref[r0:r1], rms=rms, what=f"{what} rows {r0}..{r1 - 1}")
+    return rms
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw BF16 bit patterns of a CPU BF16 tensor (what the row-parallel
+    oracle takes, at half the size of float32 values)."""
+    return t.contiguous().view(torch.int16).numpy()
+
+
 def assert_codes_equal(got, want, what):
     got = np.asarray(got, dtype=np.uint8)
     want = np.asarray(want, dtype=np.uint8)
@@ -66,15 +84,18 @@ def assert_scales_equal(got, want, what):
 
 
 def sample_rows(M, n, seed=0):
-    """Sorted sample of about n row indices touching every 128-row tile,
-    always including the first and last row."""
+    """Sorted sample of distinct row indices touching every 128-row tile:
+    about n rows spread evenly over the tiles (drawn without replacement),
+    always including the first and last row; every row when M <= n."""
+    if M <= n:
+        return np.arange(M, dtype=np.int64)
     rng = np.random.default_rng(seed)
     tiles = (M + 127) // 128
     per = max(1, n // max(tiles, 1))
     rows = set([0, M - 1])
     for t in range(tiles):
         lo, hi = t * 128, min(M, t * 128 + 128)
-        rows.update(rng.integers(lo, hi, size=min(per, hi - lo)).tolist())
+        rows.update((lo + rng.choice(hi - lo, size=min(per, hi - lo), replace=False)).tolist())
     return np.array(sorted(rows), dtype=np.int64)
 
 

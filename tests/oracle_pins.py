@@ -510,6 +510,29 @@ def pin_dequant_roundtrip(o):
     assert np.all(got == np.float32(1.1328125)), got[0, 0]
 
 
+def pin_dequant_float64(o):
+    """The float64 block dequantisation dec(q) * s on a hand-built 256 x 384
+    matrix of six blocks with six different scales: sampled elements equal
+    the exact rational product of the code's value (from the E4M3 format)
+    and its own block's scale, so a transposed, reversed or mis-broadcast
+    scale fails; and its float32 rounding, rounded to BF16, is exactly the
+    BF16 dequantisation (the float64 product of a <= 4-bit code value and a
+    float32 scale is exact)."""
+    rng = np.random.default_rng(47)
+    codes = rng.integers(0, 256, size=(256, 384)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x7E  # NaN codes are outside the contract
+    sw = np.array([[1.5, 2.0 ** -3, 3.0], [0.75, 5.0, 2.0 ** -10]], dtype=np.float32)
+    y = o.dequant_weight_128x128(codes, sw)
+    assert y.shape == (256, 384) and y.dtype == np.float64
+    pos = [(0, 0), (127, 127), (128, 0), (0, 128), (255, 383), (129, 257), (5, 300), (200, 140)]
+    pos += [tuple(p) for p in rng.integers(0, [256, 384], size=(200, 2))]
+    for n, k in pos:
+        want = _frac_dec(int(codes[n, k])) * Fraction(float(sw[n // 128, k // 128]))
+        assert Fraction(float(y[n, k])) == want, (n, k, y[n, k], float(want))
+    y16 = o.dequant_weight_128x128_bf16(codes, sw)
+    assert np.array_equal(o.bf16_round(y.astype(np.float32)).view(np.uint32), y16.view(np.uint32))
+
+
 # ---------------------------------------------------------------------------
 # Backward GEMMs
 # ---------------------------------------------------------------------------
@@ -803,6 +826,7 @@ def pin_backward_cached(o):
 
 
 ALL_PINS = [
+    pin_dequant_float64,
     pin_act_dequant,
     pin_requant_transpose_identity,
     pin_backward_cached,

@@ -42,6 +42,36 @@ def test_binding_covers_every_export():
     assert set(_declared_functions()) <= set(binding.EXPORTS)
 
 
+def test_header_preamble_discloses_owned_memory():
+    """The conventions every caller reads first name all memory the library
+    owns: the status word, the no-alloc GEMM's static array and the
+    split-K workspace pool, with its bound and stream rule."""
+    text = open(HEADER).read()
+    preamble = text[:text.index("#ifndef FP8BS_H")]
+    for phrase in ("status word", "static scratch array", "memory pool", "128 KiB per SM", "on its stream",
+                   "fp8_blockscaled_gemm_workspace_bytes"):
+        assert phrase in preamble, phrase
+    gemm_doc = text[:text.index("fp8bs_status fp8_blockscaled_gemm(")]
+    gemm_doc = gemm_doc[gemm_doc.rindex("/*"):]
+    assert "pool" in gemm_doc and "workspace" in gemm_doc
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((128, 256, 256, None), 1),        # null out
+    ((-1, 256, 256, "out"), 1),        # negative M
+    ((128, 100, 256, "out"), 3),       # N % 128
+    ((128, 256, 0, "out"), 3),         # K == 0
+    ((0, 256, 256, "out"), 0),         # M == 0: nothing to split, no device query
+])
+def test_workspace_query_validation(lib, args, expect):
+    out = ctypes.c_size_t(12345)
+    M, N, K, o = args
+    st = lib.fp8_blockscaled_gemm_workspace_bytes(M, N, K, ctypes.byref(out) if o else None)
+    assert st == expect
+    if o and expect in (0, 3):
+        assert out.value == 0
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert lib.fp8bs_status_string(code)

@@ -118,27 +118,6 @@ def test_output_guard_rows():
     assert_gemm_close(f32(ybuf)[:M], y_ref)
 
 
-@pytest.mark.parametrize("name", ["up", "down", "decode"])
-def test_full_size_sampled(name):
-    """Full-size configurations in the benchmark's launch configuration.
-    The oracle covers sampled rows (every 128-row tile) x sampled 128-column
-    blocks; rows and blocks are independent under the method's grouping, so
-    the restriction is exact."""
-    x, w = workloads.config_inputs(name)
-    y, (qa, sa, qw, sw) = fb.linear_forward(x.to(DEV), w.to(DEV))
-    torch.cuda.synchronize()
-    assert fb.fp8bs_last_device_error() == 0
-    rows = sample_rows(x.shape[0], 256, seed=21)
-    blocks = sample_blocks(w.shape[0] // 128, 6, seed=22)
-    qa_r, sa_r, qw_r, sw_r, y_ref, cols = oracle_dense_sampled(x, w, rows, blocks)
-    assert_codes_equal(u8(qa)[rows], qa_r, "qa")
-    assert_scales_equal(f32(sa)[:, rows], sa_r, "sa")
-    assert_codes_equal(u8(qw)[cols], qw_r, "qw")
-    assert_scales_equal(f32(sw)[blocks], sw_r, "sw")
-    ysub = y[torch.as_tensor(rows, device=DEV)][:, torch.as_tensor(cols, device=DEV)]
-    assert_gemm_close(f32(ysub), y_ref)
-
-
 @pytest.mark.parametrize("M,N,K", [(129, 384, 256), (300, 512, 640), (1300, 4096, 384), (64, 1024, 1024)])
 def test_f32_output(M, N, K):
     """FP32 output ("outputs in BF16 or FP32", paragraph 4): within the GEMM

@@ -11,7 +11,7 @@ import torch
 import fp8_fine_grained_14_b300 as fb
 import oracle
 from fp8_fine_grained_14_b300 import workloads
-from helpers import assert_codes_equal, assert_scales_equal, f32, sample_blocks, sample_rows, u8
+from helpers import assert_codes_equal, assert_scales_equal, f32, u8
 from oracle_pins import exact_tie_groups
 
 pytestmark = pytest.mark.gpu
@@ -224,19 +224,3 @@ def test_weight_quant_random_sweep():
     w = torch.randn(4096, 4096, generator=g)
     w = w * torch.pow(2.0, torch.randint(-40, 40, (32, 1, 32, 1), generator=g).float()).expand(32, 128, 32, 128).reshape(4096, 4096)
     _weight_parity(w.to(torch.bfloat16))
-
-
-@pytest.mark.parametrize("name", ["up", "down", "decode"])
-def test_quant_full_size_sampled(name):
-    """Full-size configurations, launched as the benchmark launches them;
-    oracle on sampled rows (every 128-row tile) and sampled weight blocks."""
-    x, w = workloads.config_inputs(name)
-    _act_parity(x, rows=sample_rows(x.shape[0], 256, seed=1))
-    _weight_parity(w, blocks=sample_blocks(w.shape[0] // 128, 6, seed=2))
-
-
-def test_quant_grouped_full_size_sampled():
-    c = workloads.CONFIGS["grouped"]
-    offsets, x, w = workloads.grouped_inputs(**{k: c[k] for k in ("tokens", "topk", "G", "N", "K")})
-    _act_parity(x, rows=sample_rows(x.shape[0], 512, seed=4))
-    _weight_parity(w, blocks=sample_blocks(w.shape[0] * w.shape[1] // 128, 8, seed=5))

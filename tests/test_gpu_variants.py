@@ -4,7 +4,9 @@ quantiser (the TileKernels release, "DeepSeek starts updating frequently",
 item "Quantification"; E5M6 in "The Definitive Information To Deepseek",
 paragraph 3).  Codes and scales bit-exact; the SwiGLU product, computed in
 FP32 with the CUDA exponential, within its rounding bound of the exact
-float64 value, and its codes bit-exact given that product."""
+float64 value, its codes bit-exact given that product, and bit-exact with
+the oracle's own end-to-end codes and scales wherever the two products
+agree."""
 import numpy as np
 import pytest
 import torch
@@ -101,9 +103,31 @@ def test_swiglu_quant(M, F):
     # the product: BF16 rounding of a float32 value within a few ulps of silu(g) * u
     guf = f32(gu)
     h64 = oracle.silu_mul(guf[:, :F], guf[:, F:])
+    h_or, q_or, s_or = oracle.swiglu_quant_act_1x128(guf)
     h_ref = oracle.bf16_round(h64.astype(np.float32))
+    assert np.array_equal(h_or.view(np.uint32), h_ref.view(np.uint32))
     differ = hg != h_ref
     assert differ.mean() < 1e-3, differ.mean()
+    # end to end against the oracle's own codes and scales: every 1x128 group
+    # whose 128 products agree with the oracle's bit for bit has the oracle's
+    # codes and scale; in a group with a differing product, the scale is the
+    # oracle's unless the group's largest magnitude differs, and where the
+    # scale agrees every code of an agreeing product agrees too
+    KB = F // 128
+    same_h = (hg.view(np.uint32) == h_or.view(np.uint32)).reshape(M, KB, 128)
+    whole = same_h.all(axis=2)
+    q_gpu, q_ref = u8(qa).reshape(M, KB, 128), q_or.reshape(M, KB, 128)
+    s_gpu, s_ref = f32(sa)[:, :M].T, s_or.T
+    assert np.array_equal(q_gpu[whole], q_ref[whole]), "codes differ in groups whose products agree"
+    assert np.array_equal(s_gpu[whole].view(np.uint32), s_ref[whole].view(np.uint32))
+    amax_same = (np.max(np.abs(hg.reshape(M, KB, 128)), axis=2) ==
+                 np.max(np.abs(h_or.reshape(M, KB, 128)), axis=2))
+    assert np.array_equal(s_gpu[amax_same].view(np.uint32), s_ref[amax_same].view(np.uint32))
+    scale_same = s_gpu.view(np.uint32) == s_ref.view(np.uint32)
+    agree = same_h & scale_same[:, :, None]
+    assert np.array_equal(q_gpu[agree], q_ref[agree]), "codes differ where product and scale agree"
+    print(f"SwiGLU {M}x{F}: {differ.mean():.2e} of the products and {1 - whole.mean():.2e} of the 1x128 groups "
+          f"differ from the oracle's (bound on products: 1e-3)")
     a = np.abs(h64[differ])
     ulp_bf16 = 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-38))) - 7)
     assert np.all(np.abs(hg[differ] - h64[differ]) <= 0.5 * ulp_bf16 + a * 2.0 ** -20)

@@ -78,6 +78,15 @@ MUTANTS = {
     "dequant_scale_of_first_block": (
         "scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float32), GROUP, axis=0), GROUP, axis=1)",
         "scale = np.full(qw.shape, np.asarray(sw, dtype=np.float32).flat[0], dtype=np.float32)"),
+    "dequant64_scale_rows_reversed": (
+        "scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float64), GROUP, axis=0), GROUP, axis=1)",
+        "scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float64)[::-1], GROUP, axis=0), GROUP, axis=1)"),
+    "dequant64_scale_of_first_block": (
+        "scale = np.repeat(np.repeat(np.asarray(sw, dtype=np.float64), GROUP, axis=0), GROUP, axis=1)",
+        "scale = np.full((N, K), np.asarray(sw, dtype=np.float64).flat[0])"),
+    "dequant64_scale_dropped": (
+        "return e4m3_decode(qw) * scale",
+        "return e4m3_decode(qw) + 0 * scale"),
     "rowscaled_column_scale_of_chunk_0": (
         "y += chunk * (sa[kb, :M].astype(np.float64)[:, None] * sb[kb, :N].astype(np.float64)[None, :])",
         "y += chunk * (sa[kb, :M].astype(np.float64)[:, None] * sb[0, :N].astype(np.float64)[None, :])"),
