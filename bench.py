@@ -178,57 +178,86 @@ def profiled_traffic(kernel, config):
 # ---------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes):
+    SM clock, maximum SM clock and the current clock event reasons."""
+
+    SM = 1  # NVML_CLOCK_SM
+
+    def __init__(self, device):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        rc = self.lib.nvmlInit_v2()
+        if rc != 0:
+            raise OSError(f"nvmlInit_v2 returned {rc}")
+        self.handle = ctypes.c_void_p()
+        rc = -1
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            rc = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle))
+        except Exception:
+            rc = -1
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device.index), ctypes.byref(self.handle))
+        if rc != 0:
+            raise OSError(f"no NVML handle for {device} ({rc})")
+        self._reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._u = ctypes.c_uint()
+        self._ull = ctypes.c_ulonglong()
+
+    def clock(self, fn="nvmlDeviceGetClockInfo"):
+        rc = getattr(self.lib, fn)(self.handle, self.SM, self.ct.byref(self._u))
+        if rc != 0:
+            raise OSError(f"{fn} returned {rc}")
+        return float(self._u.value)
+
+    def reasons(self):
+        rc = self._reasons_fn(self.handle, self.ct.byref(self._ull))
+        if rc != 0:
+            raise OSError(f"clock event reasons: {rc}")
+        return int(self._ull.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
     """Samples the SM clock and the clock event reasons of one GPU through
-    NVML (read-only queries) from a host thread, every `period_s` seconds or
-    as fast as NVML answers, while the host waits for the timed region.  A
-    10 ms region gets tens of samples (nvidia-smi's loop is 20 ms at best)."""
+    NVML (read-only queries) from a host thread, as fast as NVML answers
+    (plus `period_s`), while the host waits for the timed region.  A 10 ms
+    region gets tens of samples (nvidia-smi's loop is 20 ms at best)."""
 
-    REASONS = {"hw_slowdown": "nvmlClocksEventReasonHwSlowdown",
-               "hw_thermal_slowdown": "nvmlClocksEventReasonHwThermalSlowdown",
-               "sw_thermal_slowdown": "nvmlClocksEventReasonSwThermalSlowdown",
-               "sw_power_cap": "nvmlClocksEventReasonSwPowerCap",
-               "hw_power_brake_slowdown": "nvmlClocksEventReasonHwPowerBrakeSlowdown"}
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
     def __init__(self, device, period_s=0.0002):
         import threading
 
-        self.samples = []  # (t, sm_mhz, reasons bitmask)
+        self.samples = []  # (host time, sm_mhz, reasons bitmask)
         self.max_mhz = None
         self.error = None
         self.period_s = period_s
         self._stop = threading.Event()
         self._thread = None
         try:
-            import pynvml
-
-            self.nv = pynvml
-            pynvml.nvmlInit()
-            self.handle = self._handle(device)
-            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle, pynvml.NVML_CLOCK_SM))
-            self.bits = {k: getattr(pynvml, v, 0) for k, v in self.REASONS.items()}
+            self.nv = _Nvml(device)
+            self.max_mhz = self.nv.clock("nvmlDeviceGetMaxClockInfo")
         except Exception as e:  # no NVML: report unsampled
             self.error = f"{type(e).__name__}: {e}"
             self.nv = None
 
-    def _handle(self, device):
-        nv = self.nv
-        try:
-            uuid = str(torch.cuda.get_device_properties(device).uuid)
-            return nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
-        except Exception:
-            return nv.nvmlDeviceGetHandleByIndex(device.index)
-
     def _run(self):
-        nv, h = self.nv, self.handle
         while not self._stop.is_set():
             try:
-                mhz = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                mhz, reasons = self.nv.clock(), self.nv.reasons()
             except Exception as e:  # pragma: no cover
                 self.error = f"{type(e).__name__}: {e}"
                 return
-            self.samples.append((time.perf_counter(), float(mhz), int(reasons)))
+            self.samples.append((time.perf_counter(), mhz, reasons))
             if self.period_s:
                 time.sleep(self.period_s)
 
@@ -249,7 +278,7 @@ class ClockSampler:
             self._thread.join(timeout=5)
         if self.nv is not None:
             try:
-                self.nv.nvmlShutdown()
+                self.nv.close()
             except Exception:
                 pass
 
@@ -261,14 +290,10 @@ class ClockSampler:
         if not sel:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0,
                     "source": "nvml" if self.nv is not None else f"unavailable ({self.error})"}
-        seen = set()
-        for _, _, r in sel:
-            for name, bit in self.bits.items():
-                if bit and r & bit:
-                    seen.add(name)
+        seen = sorted(name for name, bit in self.REASONS.items() if any(r & bit for _, _, r in sel))
         med = statistics.median(m for _, m, _ in sel)
         out = {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "sm_mhz_min": min(m for _, m, _ in sel),
-               "reasons": sorted(seen), "samples": len(sel), "source": "nvml, read-only, sampled in a host thread"}
+               "reasons": seen, "samples": len(sel), "source": "NVML (read-only) polled from a host thread"}
         if ms is not None:
             out["region_ms_x_median_mhz"] = ms * med
         return out

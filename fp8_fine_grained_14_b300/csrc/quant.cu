@@ -34,7 +34,7 @@ namespace {
 // 2U loads of a thread are issued before any arithmetic.
 // ---------------------------------------------------------------------------
 template <int U>
-__global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint4* __restrict__ x, int64_t M, int64_t KB,
+__global__ void __launch_bounds__(256, 6) quant_act_1x128_kernel(const uint4* __restrict__ x, int64_t M, int64_t KB,
                                                               int64_t ldx_v, uint4* __restrict__ q, int64_t ldq_v,
                                                               float* __restrict__ sa, int64_t ld_sa) {
   const int lane8 = threadIdx.x & 7;
