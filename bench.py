@@ -25,7 +25,11 @@ With --impl reference the CPU oracle itself is timed, one bounded sample of
 the workload per step, on this host's cores (rank 0 only).
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
-torch.cuda.synchronize(); the maximum over ranks is reported.  No L2 flush:
+torch.cuda.synchronize(), timed by CUDA events on the launching stream; the
+maximum over ranks is reported.  The K steps are replayed from a CUDA graph
+of their C-ABI calls (--no-graph: stream launches).  Per-kernel times come
+from a second pass of K stream-launched steps with a CUDA event after every
+kernel, so each includes the launch gap before its kernel.  No L2 flush:
 every step's working set (inputs, codes, scales, output) is several times the
 126 MB L2.  Multi-GPU runs are independent replicas (weak scaling): the
 linear layer needs no exchange between ranks.
@@ -434,42 +438,92 @@ class Step:
         return 2 * M * N * K, "tensor"
 
 
-def time_device(step, stream, steps, warmup, dist, device):
+def capture_steps(step, stream, steps):
+    """The C-ABI calls of `steps` steps recorded into one CUDA graph (the
+    kernels, their arguments and their order; the library's host-side
+    validation and tensor-map encoding run once, at capture).  Replaying it
+    launches exactly the kernels that the stream-launched steps launch, with
+    about 1 us between dependent kernels instead of the 3-6 us of separate
+    stream launches.  Returns None when the calls cannot be captured."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for _ in range(steps):
+                step.run()
+        return g
+    except Exception as e:  # e.g. an allocation the capture does not accept
+        torch.cuda.synchronize()
+        print(f"note: the step could not be captured in a CUDA graph ({type(e).__name__}: {e}); "
+              "timing stream launches", file=sys.stderr)
+        return None
+
+
+def time_device(step, stream, steps, warmup, dist, device, use_graph=True):
+    """The timed region: `steps` steps bracketed by a barrier and a device
+    synchronisation on both sides, timed by CUDA events on the launching
+    stream; the steps are replayed from a CUDA graph of the same C-ABI calls
+    (stream-launched when capture is unavailable or disabled).
+
+    Per-kernel durations then come from a second pass of `steps`
+    stream-launched steps with a CUDA event recorded after every kernel: a
+    kernel's duration runs from the previous event to its own, so it includes
+    the launch gap before the kernel (3-6 us on B300) and never understates
+    the kernel."""
     for _ in range(warmup):
         with torch.cuda.stream(stream):
             step.run()
     torch.cuda.synchronize(device)
     if step.fb.fp8bs_last_device_error(stream) != 0:
         raise RuntimeError("device status word set during warm-up")
+    graph = capture_steps(step, stream, steps) if use_graph else None
+    launch_mode = "CUDA graph of the steps' C-ABI calls" if graph is not None else "stream launches"
+    if graph is not None:
+        graph.replay()  # untimed: uploads the graph
+        torch.cuda.synchronize(device)
     sampler = ClockSampler(device)
     sampler.start()
     barrier(dist, device)
     torch.cuda.synchronize(device)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    events = []
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(steps):
-            step.run(events)
+        if graph is not None:
+            graph.replay()
+        else:
+            for _ in range(steps):
+                step.run()
         end.record(stream)
     torch.cuda.synchronize(device)
     t1 = time.perf_counter()
     barrier(dist, device)
     sampler.stop()
     total_ms = start.elapsed_time(end)
+    status = step.fb.fp8bs_last_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device status word {status} after the timed region")
+    del graph
+    # per-kernel attribution pass
+    events = []
+    a = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            step.run(events)
+    torch.cuda.synchronize(device)
     nk = len(step.kernels)
     per_kernel = {k: 0.0 for k in step.kernels}
-    prev = start
+    prev = a
     for i, ev in enumerate(events):
         per_kernel[step.kernels[i % nk]] += prev.elapsed_time(ev)
         prev = ev
     per_kernel = {k: v / steps for k, v in per_kernel.items()}
+    attribution_ms = a.elapsed_time(events[-1]) / steps
     status = step.fb.fp8bs_last_device_error(stream)
     if status != 0:
-        raise RuntimeError(f"device status word {status} after the timed region")
-    return total_ms, per_kernel, sampler.summary(t0, t1, total_ms)
+        raise RuntimeError(f"device status word {status} after the attribution pass")
+    return total_ms, per_kernel, sampler.summary(t0, t1, total_ms), attribution_ms, launch_mode
 
 
 def time_e2e(name, inp, step, stream, steps, warmup, device, fb):
@@ -904,7 +958,8 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     step = Step(name, inp, device, stream, fb)
 
-    total_ms, per_kernel, clocks = time_device(step, stream, args.steps, args.warmup, dist, device)
+    total_ms, per_kernel, clocks, attribution_ms, launch_mode = time_device(
+        step, stream, args.steps, args.warmup, dist, device, use_graph=not args.no_graph)
     total_ms = max_over_ranks(dist, total_ms, device)
     ms_per_step = total_ms / args.steps
     flops = step.flops()
@@ -966,6 +1021,10 @@ def run_ours(args):
             "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for k, v in kern.items()},
             "tflops_gemm_only": flops / (per_kernel[step.kernels[-1]] * 1e-3) / 1e12,
+            "timing": {"timed_region": f"{args.steps} steps, {launch_mode}, CUDA events on the launching stream",
+                       "kernels": f"a second pass of {args.steps} stream-launched steps with a CUDA event after "
+                                  "each kernel; a kernel's time includes the launch gap before it",
+                       "attribution_pass_ms_per_step": attribution_ms},
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": step_launches(step, torch.cuda.get_device_properties(device).multi_processor_count)
@@ -986,6 +1045,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time stream launches instead of a CUDA graph of the step's calls")
     ap.add_argument("--rows", action="store_true",
                     help="time every scope-table kernel on its own (one JSON line per row) and exit")
     ap.add_argument("--only", default="",

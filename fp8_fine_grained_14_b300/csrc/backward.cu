@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(256, TQuant<FROM_FP8>::kCtasPerSm) quant_act_1
                                                                    int64_t ld_s, const float* __restrict__ sa,
                                                                    int64_t ld_sa, unsigned* status,
                                                                    uint64_t timeout_ns) {
+  pdl_wait();
   constexpr int kTStages = TQuant<FROM_FP8>::kStages;
   constexpr int kTTileBytes = TQuant<FROM_FP8>::kTileBytes;
   constexpr int kScaleBytes = TQuant<FROM_FP8>::kScaleBytes;
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(256) transpose_weight_128x128_kernel(const uin
                                                                        const float* __restrict__ sw,
                                                                        uint4* __restrict__ qt, int64_t ldqt_v,
                                                                        float* __restrict__ swt) {
+  pdl_wait();
   __shared__ __align__(16) uint8_t blk[128 * 128];
   const int cg = threadIdx.x & 31;  // input columns 4 cg .. 4 cg + 3 = output rows
   const int rg = threadIdx.x >> 5;  // input rows 16 rg .. 16 rg + 15 = output columns
@@ -241,7 +243,7 @@ cudaError_t launch_quant_t(const DeviceInfo& dev, const CUtensorMap& tmX, int64_
   const int64_t tiles = MB * KB;
   const int64_t resident = static_cast<int64_t>(dev.num_sms) * TQuant<FROM_FP8>::kCtasPerSm;
   const int grid = static_cast<int>(tiles < resident ? tiles : resident);
-  quant_act_1x128_t_kernel<FROM_FP8><<<grid, 256, kSmem, stream>>>(
+  (void)launch_pdl(quant_act_1x128_t_kernel<FROM_FP8>, grid, 256, kSmem, stream,
       tmX, MB, KB, static_cast<uint4*>(qt), ldqt / 16, st, ld_st, sa, ld_sa, dev.status, wait_timeout_ns());
   return cudaGetLastError();
 }
@@ -269,7 +271,7 @@ cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q
   (void)dev;
   const int64_t NB = N / 128, KB = K / 128;
   const dim3 grid(static_cast<unsigned>(NB), static_cast<unsigned>(KB < kMaxGridY ? KB : kMaxGridY));
-  transpose_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
+  (void)launch_pdl(transpose_weight_128x128_kernel, grid, 256, 0, stream, static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
                                                             static_cast<uint4*>(qt), ldqt / 16, swt);
   return cudaGetLastError();
 }

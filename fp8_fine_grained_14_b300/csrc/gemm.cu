@@ -338,6 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touches only this CTA's (or pair's) shared and tensor
+  // memory; from here on the kernel reads and writes global memory.
+  pdl_wait();
   // The pair's full and tempty barriers live in the leader.
   const uint32_t full_base = CG > 1 ? map_shared_rank(bar_full, 0) : bar_full;
   const uint32_t tempty_base = CG > 1 ? map_shared_rank(bar_tempty, 0) : bar_tempty;
@@ -694,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // t % 32.
 template <int BN, int CG, bool F32>
 __global__ void __launch_bounds__(256) split_tail_reduce_kernel(const Params p) {
+  pdl_wait();
   constexpr int kHalfCols = BN / 2;
   constexpr int64_t kRegion = 8 * kHalfCols;  // float4 per warp region
   const int32_t region = static_cast<int32_t>(blockIdx.x % kEpiWarps);
@@ -782,17 +786,19 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   }
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = CG;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kDynamic;
   cfg.stream = stream;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3(CG, 1, 1);
   const int resident = max_resident_clusters<BN, STAGES, GROUPED, CG, F32, RS, HALF_A, RES>(dev, cfg);
   Params p = p0;
@@ -848,7 +854,7 @@ cudaError_t launch_kernel(const DeviceInfo& dev, const CUtensorMap& tmA, const C
   e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmY, p);
   if (e == cudaSuccess && p.split > 1) {
     const unsigned blocks = static_cast<unsigned>((p.n_items - p.t_full) / p.split) * CG * kEpiWarps;
-    split_tail_reduce_kernel<BN, CG, F32><<<blocks, 256, 0, stream>>>(p);
+    (void)launch_pdl(split_tail_reduce_kernel<BN, CG, F32>, blocks, 256, 0, stream, p);
     e = cudaGetLastError();
   }
   if (owned) {

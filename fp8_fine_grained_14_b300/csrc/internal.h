@@ -8,6 +8,27 @@
 
 namespace fp8bs {
 
+// Launches `kernel` with programmatic stream serialisation: the launch may
+// be processed while the previous kernel on `stream` is still running, which
+// shortens the gap between dependent kernels (about 1 us instead of 3-6 us
+// on B300).  Every kernel of the library starts with pdl_wait() (ptx.cuh), so
+// it still sees all the writes of the work before it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct DeviceInfo {
   int ordinal;
   int num_sms;

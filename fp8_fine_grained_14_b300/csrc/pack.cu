@@ -12,6 +12,7 @@
 // Deepseek", "Figure 7 (a)" item (2): one scale per 128x128 block); only the
 // byte order changes.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fp8bs {
 namespace {
@@ -20,6 +21,7 @@ namespace {
 // (chunks 4 (t % 2) .. + 3) to their swizzled positions in the block's image.
 __global__ void __launch_bounds__(256) pack_weight_128x128_kernel(const uint4* __restrict__ q, int64_t NB,
                                                                   int64_t KB, int64_t ldq_v, uint4* __restrict__ wp) {
+  pdl_wait();
   const int r = threadIdx.x >> 1;
   const int h = threadIdx.x & 1;
   for (int64_t tile = blockIdx.x; tile < NB * KB; tile += gridDim.x) {
@@ -41,7 +43,7 @@ cudaError_t launch_pack_weight_128x128(const DeviceInfo& dev, const void* q, int
   const int64_t NB = N / 128, KB = K / 128;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
   const int64_t tiles = NB * KB;
-  pack_weight_128x128_kernel<<<static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0, stream>>>(
+  (void)launch_pdl(pack_weight_128x128_kernel, static_cast<unsigned>(tiles < cap ? tiles : cap), 256, 0, stream,
       static_cast<const uint4*>(q), NB, KB, ldq / 16, static_cast<uint4*>(wp));
   return cudaGetLastError();
 }

@@ -22,6 +22,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: every kernel of the library is launched so
+// that its launch may be processed while the previous kernel of the stream is
+// still finishing, and waits here, before its first global memory access,
+// until that kernel has completed and its writes are visible.  Without a
+// preceding kernel launched that way the wait returns at once, so stream
+// order is kept in every case.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Record a device-side failure: first writer wins.
 __device__ __forceinline__ void record_status(unsigned* status, unsigned code) {
   atomicCAS(status, 0u, code);

@@ -37,6 +37,7 @@ template <int U>
 __global__ void __launch_bounds__(256, 6) quant_act_1x128_kernel(const uint4* __restrict__ x, int64_t M, int64_t KB,
                                                               int64_t ldx_v, uint4* __restrict__ q, int64_t ldq_v,
                                                               float* __restrict__ sa, int64_t ld_sa) {
+  pdl_wait();
   const int lane8 = threadIdx.x & 7;
   const int r = threadIdx.x >> 3;  // 32 rows per CTA
   const int64_t kb0 = static_cast<int64_t>(blockIdx.x) * U;
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(256, 3) quant_weight_128x128_kernel(const uint
                                                                       int64_t KB, int64_t ldw_v,
                                                                       uint2* __restrict__ q, int64_t ldq_v,
                                                                       float* __restrict__ sw) {
+  pdl_wait();
   __shared__ uint32_t warp_max[8];
   const int c = threadIdx.x & 15;
   const int r0 = threadIdx.x >> 4;
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(256) dequant_weight_128x128_kernel(const uint4
                                                                      int64_t KB, int64_t ldq_v,
                                                                      const float* __restrict__ sw,
                                                                      uint4* __restrict__ y, int64_t ldy_v) {
+  pdl_wait();
   const int c = threadIdx.x & 7;
   const int r0 = threadIdx.x >> 3;
   const int64_t kb = blockIdx.x;
@@ -180,7 +183,7 @@ cudaError_t launch_quant_act_1x128(const DeviceInfo& dev, const void* x, int64_t
   const int64_t tiles_m = (M + 31) / 32;
   const dim3 grid(static_cast<unsigned>((KB + kUnroll - 1) / kUnroll),
                   static_cast<unsigned>(tiles_m < kMaxGridY ? tiles_m : kMaxGridY));
-  quant_act_1x128_kernel<kUnroll><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), M, KB, ldx / 8,
+  (void)launch_pdl(quant_act_1x128_kernel<kUnroll>, grid, 256, 0, stream, static_cast<const uint4*>(x), M, KB, ldx / 8,
                                                             static_cast<uint4*>(q), ldq / 16, sa, ld_sa);
   return cudaGetLastError();
 }
@@ -190,7 +193,7 @@ cudaError_t launch_quant_weight_128x128(const DeviceInfo& dev, const void* w, in
   (void)dev;
   const int64_t NB = N / 128, KB = K / 128;
   const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(NB < kMaxGridY ? NB : kMaxGridY));
-  quant_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(w), NB, KB, ldw / 8,
+  (void)launch_pdl(quant_weight_128x128_kernel, grid, 256, 0, stream, static_cast<const uint4*>(w), NB, KB, ldw / 8,
                                                         static_cast<uint2*>(q), ldq / 8, sw);
   return cudaGetLastError();
 }
@@ -201,7 +204,7 @@ cudaError_t launch_dequant_weight_128x128(const DeviceInfo& dev, const void* q, 
   const int64_t NB = N / 128, KB = K / 128;
   const int64_t pairs = (NB + 1) / 2;
   const dim3 grid(static_cast<unsigned>(KB), static_cast<unsigned>(pairs < kMaxGridY ? pairs : kMaxGridY));
-  dequant_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
+  (void)launch_pdl(dequant_weight_128x128_kernel, grid, 256, 0, stream, static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
                                                           static_cast<uint4*>(y), ldy / 8);
   return cudaGetLastError();
 }

@@ -26,6 +26,7 @@ template <int U>
 __global__ void __launch_bounds__(256) quant_per_token_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
                                                               int64_t ldx_v, uint2* __restrict__ q, int64_t ldq_v,
                                                               float* __restrict__ s) {
+  pdl_wait();
   __shared__ uint32_t warp_max[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(256) quant_per_token_kernel(const uint4* __res
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) channel_absmax_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
                                                              int64_t ldx_v, uint32_t* __restrict__ amax_bits) {
+  pdl_wait();
   __shared__ uint32_t part[8][32 * 4];  // [row slot][packed column pairs]
   const int lane = threadIdx.x & 31, r8 = threadIdx.x >> 5;
   const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
@@ -107,6 +109,7 @@ __global__ void __launch_bounds__(256) channel_absmax_kernel(const uint4* __rest
 __global__ void __launch_bounds__(256) quant_per_channel_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
                                                                 int64_t ldx_v, const uint32_t* __restrict__ amax_bits,
                                                                 uint2* __restrict__ q, int64_t ldq_v) {
+  pdl_wait();
   const int lane = threadIdx.x & 31, r8 = threadIdx.x >> 5;
   const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   if (col_v >= KV) return;
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(256) quant_per_channel_cluster_kernel(const ui
                                                                         int64_t KV, int64_t ldx_v,
                                                                         uint2* __restrict__ q, int64_t ldq_v,
                                                                         float* __restrict__ s) {
+  pdl_wait();
   __shared__ uint32_t warp_max[8][8][4];            // [warp][channel group][BF16 pair]
   __shared__ __align__(16) uint32_t cta_max[8][4];  // [channel group][BF16 pair]: this CTA's maxima
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(256) quant_per_channel_cluster_kernel(const ui
 }
 
 __global__ void channel_scales_kernel(uint32_t* __restrict__ amax_bits_to_scales, int64_t K) {
+  pdl_wait();
   const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (k < K) {
     const float amax = __uint_as_float(amax_bits_to_scales[k] << 16);
@@ -246,6 +251,7 @@ __global__ void channel_scales_kernel(uint32_t* __restrict__ amax_bits_to_scales
 }
 
 __global__ void zero_words_kernel(uint32_t* __restrict__ p, int64_t n) {
+  pdl_wait();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0u;
 }
@@ -313,6 +319,7 @@ __device__ __forceinline__ uint32_t e5m6_encode2(uint32_t w) {
 // (t, t + 256, ..) of a block before coding any of them.
 __global__ void __launch_bounds__(256) cast_e5m6_kernel(const uint4* __restrict__ x, int64_t nv,
                                                         uint4* __restrict__ out) {
+  pdl_wait();
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * 1024; b < nv; b += static_cast<int64_t>(gridDim.x) * 1024) {
     uint4 v[4];
 #pragma unroll
@@ -331,6 +338,7 @@ __global__ void __launch_bounds__(256) cast_e5m6_kernel(const uint4* __restrict_
 
 __global__ void __launch_bounds__(256) e5m6_to_bf16_kernel(const uint4* __restrict__ c, int64_t nv,
                                                            uint4* __restrict__ out) {
+  pdl_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < nv;
        i += static_cast<int64_t>(gridDim.x) * 256) {
     const uint4 v = ld_nc_v4(c + i);
@@ -381,6 +389,7 @@ __global__ void __launch_bounds__(256) swiglu_quant_kernel(const uint4* __restri
                                                            int64_t ld_v, uint4* __restrict__ q, int64_t ldq_v,
                                                            float* __restrict__ sa, int64_t ld_sa,
                                                            uint4* __restrict__ h_out, int64_t ldh_v) {
+  pdl_wait();
   const int lane8 = threadIdx.x & 7;
   const int r = threadIdx.x >> 3;  // 32 rows per CTA
   const int64_t fb0 = static_cast<int64_t>(blockIdx.x) * U;
@@ -435,33 +444,35 @@ cudaError_t launch_quant_per_token(const DeviceInfo& dev, const void* x, int64_t
   const uint4* xv = static_cast<const uint4*>(x);
   uint2* qv = static_cast<uint2*>(q);
 if (KV <= 256)
-    quant_per_token_kernel<1><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+    (void)launch_pdl(quant_per_token_kernel<1>, grid, 256, 0, stream, xv, M, KV, ldx / 8, qv, ldq / 8, s);
   else if (KV <= 512)
-    quant_per_token_kernel<2><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+    (void)launch_pdl(quant_per_token_kernel<2>, grid, 256, 0, stream, xv, M, KV, ldx / 8, qv, ldq / 8, s);
   else if (KV <= 1024)
-    quant_per_token_kernel<4><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+    (void)launch_pdl(quant_per_token_kernel<4>, grid, 256, 0, stream, xv, M, KV, ldx / 8, qv, ldq / 8, s);
   else if (KV <= 2048)
-    quant_per_token_kernel<8><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+    (void)launch_pdl(quant_per_token_kernel<8>, grid, 256, 0, stream, xv, M, KV, ldx / 8, qv, ldq / 8, s);
   else
-    quant_per_token_kernel<16><<<grid, 256, 0, stream>>>(xv, M, KV, ldx / 8, qv, ldq / 8, s);
+    (void)launch_pdl(quant_per_token_kernel<16>, grid, 256, 0, stream, xv, M, KV, ldx / 8, qv, ldq / 8, s);
   return cudaGetLastError();
 }
 
 template <int R>
 cudaError_t launch_per_channel_cluster(const void* x, int64_t M, int64_t KV, int64_t ldx, void* q, int64_t ldq,
                                        float* s, cudaStream_t stream) {
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = kPcCluster;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((KV + 7) / 8 * kPcCluster), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, quant_per_channel_cluster_kernel<R>, static_cast<const uint4*>(x), M, KV, ldx / 8,
                             static_cast<uint2*>(q), ldq / 8, s);
 }
@@ -484,14 +495,14 @@ cudaError_t launch_quant_per_channel(const DeviceInfo& dev, const void* x, int64
     e = launch_per_channel_cluster<16>(x, M, KV, ldx, q, ldq, s, stream);
   if (e != cudaErrorNotSupported) return e == cudaSuccess ? cudaGetLastError() : e;
   uint32_t* bits = reinterpret_cast<uint32_t*>(s);
-  zero_words_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(bits, K);
+  (void)launch_pdl(zero_words_kernel, static_cast<unsigned>((K + 255) / 256), 256, 0, stream, bits, K);
   const int64_t row_tiles = (M + 63) / 64;
   const dim3 grid(static_cast<unsigned>((KV + 31) / 32),
                   static_cast<unsigned>(row_tiles < kMaxGridY ? row_tiles : kMaxGridY));
-  channel_absmax_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), M, KV, ldx / 8, bits);
-  quant_per_channel_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), M, KV, ldx / 8, bits,
+  (void)launch_pdl(channel_absmax_kernel, grid, 256, 0, stream, static_cast<const uint4*>(x), M, KV, ldx / 8, bits);
+  (void)launch_pdl(quant_per_channel_kernel, grid, 256, 0, stream, static_cast<const uint4*>(x), M, KV, ldx / 8, bits,
                                                      static_cast<uint2*>(q), ldq / 8);
-  channel_scales_kernel<<<static_cast<unsigned>((K + 255) / 256), 256, 0, stream>>>(bits, K);
+  (void)launch_pdl(channel_scales_kernel, static_cast<unsigned>((K + 255) / 256), 256, 0, stream, bits, K);
   return cudaGetLastError();
 }
 
@@ -499,7 +510,7 @@ cudaError_t launch_cast_e5m6(const DeviceInfo& dev, const void* x, int64_t n, vo
   const int64_t nv = n / 8;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
   const int64_t blocks = (nv + 1023) / 1024;
-  cast_e5m6_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
+  (void)launch_pdl(cast_e5m6_kernel, static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream,
       static_cast<const uint4*>(x), nv, static_cast<uint4*>(codes));
   return cudaGetLastError();
 }
@@ -508,7 +519,7 @@ cudaError_t launch_e5m6_to_bf16(const DeviceInfo& dev, const void* codes, int64_
   const int64_t nv = n / 8;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
   const int64_t blocks = (nv + 255) / 256;
-  e5m6_to_bf16_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
+  (void)launch_pdl(e5m6_to_bf16_kernel, static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream,
       static_cast<const uint4*>(codes), nv, static_cast<uint4*>(y));
   return cudaGetLastError();
 }
@@ -522,7 +533,7 @@ cudaError_t launch_swiglu_quant_act_1x128(const DeviceInfo& dev, const void* gat
   const int64_t tiles_m = (M + 31) / 32;
   const dim3 grid(static_cast<unsigned>((FB + kUnroll - 1) / kUnroll),
                   static_cast<unsigned>(tiles_m < kMaxGridY ? tiles_m : kMaxGridY));
-  swiglu_quant_kernel<kUnroll><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(gate_up), M, FB, ld / 8,
+  (void)launch_pdl(swiglu_quant_kernel<kUnroll>, grid, 256, 0, stream, static_cast<const uint4*>(gate_up), M, FB, ld / 8,
                                                          static_cast<uint4*>(q), ldq / 16, sa, ld_sa,
                                                          static_cast<uint4*>(h), ldh / 8);
   return cudaGetLastError();
