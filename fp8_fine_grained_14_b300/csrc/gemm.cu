@@ -12,8 +12,9 @@
 //               K chunk into a STAGES-deep shared-memory ring (mbarrier
 //               full/empty)
 //   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma kind::f8f6f4
-//               (K = 32 each) per chunk into TMEM buffer (chunk & 1), then
-//               tcgen05.commit to free the smem stage and publish the chunk
+//               (K = 32 each) per chunk into the next TMEM buffer, then one
+//               tcgen05.commit that publishes the chunk (the first promotion
+//               warp then frees the chunk's shared-memory stage)
 //   warps 2..3  idle (their warpgroup gives registers to the promotion warps)
 //   warps 4..11 promotion: tcgen05.ld the chunk (one row per thread, 64
 //               columns per load), acc += chunk * (sa[kb][m] * sw[nb][kb])
@@ -157,6 +158,18 @@ __device__ __forceinline__ void dense_tile_origin(const Params& p, int64_t tile,
   n0 = nt * BN;
 }
 
+// Accumulator buffers in tensor memory, each 128 lanes x BN FP32 columns
+// holding one K chunk.  Two 256-wide buffers fill the 512 columns, so the
+// MMAs of a 256-wide tile run at most one chunk ahead of promotion.  (Four
+// 128-wide buffers with 256 x 128 pair tiles would let them run three
+// chunks ahead, but such tiles double the operand bytes per FLOP through
+// L2 and ran the up-projection GEMM 1.57x slower; narrow tiles measured
+// the same with two or four buffers.)
+template <int BN, int CG>
+__host__ __device__ constexpr int num_tmem_bufs() {
+  return 2;
+}
+
 // Shared-memory layout.  Stage s holds its A tile at a_off(s) and its share
 // of the B tile at b_off(s).  HALF_A (M <= 64): only 64 rows of A are loaded
 // and each stage is laid out [A 8 KB][B], so the M = 128 MMA's read of A rows
@@ -175,8 +188,8 @@ struct Smem {
   static constexpr int kOffColScale = kOffStaging + kEpiWarps * kStagingBytes;
   static constexpr int kColScaleBytes = RS ? kEpiWarps * 2 * (BN / 2) * 4 : 0;
   static constexpr int kOffBar = kOffColScale + kColScaleBytes;
-  // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2]
-  static constexpr int kOffSlot = kOffBar + (2 * STAGES + 4) * 8;
+  // full[STAGES], empty[STAGES], tmem_full[NBUF], tmem_empty[NBUF]
+  static constexpr int kOffSlot = kOffBar + (2 * STAGES + 2 * num_tmem_bufs<BN, CG>()) * 8;
   static constexpr int kOffAbort = kOffSlot + 4;
   static constexpr int kBytes = kOffAbort + 4;
   static constexpr int kDynamic = kBytes + 1024;  // + alignment slack
@@ -278,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(!(RS && GROUPED), "row-scaled B is a dense-only variant");
   static_assert(!RES || (!GROUPED && !RS && !F32), "the residual epilogue is a dense BF16-output variant");
   static_assert(CG == 1 || CG == 2, "single CTAs or CTA pairs");
-  constexpr int kTmemCols = 2 * BN;   // two accumulator buffers of this CTA's 128 rows x BN
+  constexpr int NBUF = num_tmem_bufs<BN, CG>();
+  constexpr int kTmemCols = NBUF * BN;  // NBUF accumulator buffers of this CTA's 128 rows x BN
   constexpr int kHalfCols = BN / 2;   // columns per promotion warp
   constexpr uint32_t kStageTx = CG * (L::kA + L::kB);  // bytes landing per stage (whole pair)
   constexpr uint32_t kIdesc = idesc_e4m3_f32(BM * CG, BN);
@@ -296,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_full = base + L::kOffBar;
   const uint32_t bar_empty = bar_full + STAGES * 8;
   const uint32_t bar_tfull = bar_empty + STAGES * 8;
-  const uint32_t bar_tempty = bar_tfull + 2 * 8;
+  const uint32_t bar_tempty = bar_tfull + NBUF * 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kOffSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffAbort);
 
@@ -308,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);   // the leader's producer arrives; all loads of the pair credit bytes
-      mbar_init(bar_empty + 8 * s, 1);  // released by the (leader's) MMA commit
+      mbar_init(bar_empty + 8 * s, 1);  // released by this CTA's first promotion warp (see below)
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, kEpiWarps * CG);  // every promotion warp of the pair
     }
@@ -439,26 +453,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               mma_f8f6f4_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
           }
-          if (CG == 1) {
-            mma_commit(bar_empty + 8 * stage);  // smem stage reusable once these MMAs finish
-            mma_commit(bar_tfull + 8 * buf);    // chunk kb ready in TMEM buffer `buf`
-          } else {
-            mma_commit_pair(bar_empty + 8 * stage, kPairMask);  // both CTAs' stages
-            mma_commit_pair(bar_tfull + 8 * buf, kPairMask);    // both CTAs' accumulator rows
-          }
+          // One commit per chunk: chunk kb is in TMEM buffer `buf` (for a pair,
+          // in both CTAs' accumulator rows).  The same completion frees the
+          // operand stage, which the promotion side releases when it sees the
+          // commit: a second commit per chunk would cost the tensor pipe more
+          // than the later release costs the producer, which runs stages ahead.
+          if (CG == 1)
+            mma_commit(bar_tfull + 8 * buf);
+          else
+            mma_commit_pair(bar_tfull + 8 * buf, kPairMask);
           committed |= 1u << buf;
           committed_parity = (committed_parity & ~(1u << buf)) | (bphase << buf);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
-          buf ^= 1u;
-          if (buf == 0) bphase ^= 1u;
+          if (++buf == NBUF) {
+            buf = 0;
+            bphase ^= 1u;
+          }
         }
       }
       if (!ok) {
         // No MMA may still be writing TMEM when it is released.
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < NBUF; ++b)
           if (committed & (1u << b))
             (void)mbar_wait(bar_tfull + 8 * b, (committed_parity >> b) & 1u, nullptr, p.timeout_ns);
       }
@@ -472,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t staging = base + L::kOffStaging + epi * kStagingBytes;
     uint8_t* staging_ptr = smem + L::kOffStaging + epi * kStagingBytes;
     uint32_t buf = 0, bphase = 0;
+    uint32_t rel_stage = 0;  // operand stage of the next chunk (the producer's order)
     bool ok = true;
     const bool live = !HALF_A || q < 2;  // the warp's TMEM lanes can hold output rows
     while (ok && tiles.get(a_row, row_end, b_row, n0, group, kb0, kb1, unit)) {
@@ -526,6 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        // The chunk's MMAs have completed, so they no longer read this CTA's
+        // operand stage: hand it back to the producer.
+        if (epi == 0 && lane == 0) mbar_arrive(bar_empty + 8 * rel_stage);
+        if (++rel_stage == STAGES) rel_stage = 0;
         tc_fence_after_sync();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + half * kHalfCols;
         if (!live) {
@@ -584,8 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v = 0; v < kColVec; ++v) cs_next[v] = __ldg(sb_col + static_cast<int64_t>(k2) * p.ld_sb + v);
           __syncwarp();
         }
-        buf ^= 1u;
-        if (buf == 0) bphase ^= 1u;
+        if (++buf == NBUF) {
+          buf = 0;
+          bphase ^= 1u;
+        }
       }
       if (!ok) break;
 
@@ -879,6 +904,7 @@ static_assert(Smem<256, kStagesPairRS, 2, true>::kDynamic <= 232448, "shared mem
 static_assert(Smem<256, kStages256RS, 1, true>::kDynamic <= 232448, "shared memory budget (BN=256, RS)");
 static_assert(Smem<128, kStages128RS, 1, true>::kDynamic <= 232448, "shared memory budget (BN=128, RS)");
 static_assert(Smem<256, kStagesPair, 2>::kDynamic <= 232448, "shared memory budget (BN=256, pair)");
+
 static_assert(Smem<256, kStages256, 1>::kDynamic <= 232448, "shared memory budget (BN=256)");
 static_assert(Smem<128, kStages128, 1>::kDynamic <= 232448, "shared memory budget (BN=128)");
 static_assert(Smem<128, kStages128HalfA, 1, false, true>::kDynamic <= 232448, "shared memory budget (64-row A)");
