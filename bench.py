@@ -11,11 +11,12 @@ already resident in HBM:
                        quantisation of W, block-scaled GEMM -> Y (BF16);
   * grouped          : the same over 64 expert row groups, grouped GEMM;
   * decode           : activation quantisation + GEMM (W quantised once,
-                       before timing, as the workload specifies).
+                       before timing, as the workload specifies, and packed
+                       into the GEMM's stage images then as well).
 The default workload is the up-projection X[4096, 7168] x W[18432, 7168].
 
 Printed (rank 0, one JSON line): whole-job TFLOP/s (2MNK per step, all
-ranks, the step's quantisation included), per-kernel CUDA-event times, the
+ranks, the step's quantisation included), per-kernel times, the
 roofline of the dominant kernel against the measured peaks, SM clocks sampled
 during the timed region, an end-to-end figure through the C ABI with pinned
 host buffers (host->device inputs and device->host Y inside the timed
@@ -28,8 +29,11 @@ Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize(), timed by CUDA events on the launching stream; the
 maximum over ranks is reported.  The K steps are replayed from a CUDA graph
 of their C-ABI calls (--no-graph: stream launches).  Per-kernel times come
-from a second pass of K stream-launched steps with a CUDA event after every
-kernel, so each includes the launch gap before its kernel.  No L2 flush:
+from two more passes: K stream-launched steps with a CUDA event after every
+kernel (us_events: each includes the full launch gap that the event puts
+before its kernel), and the K steps as a graph with a device-timestamp kernel
+after every kernel (us_in_step: each kernel's share of the step as the graph
+runs it, plus one short launch for the stamp).  No L2 flush:
 every step's working set (inputs, codes, scales, output) is several times the
 126 MB L2.  Multi-GPU runs are independent replicas (weak scaling): the
 linear layer needs no exchange between ranks.
@@ -55,6 +59,7 @@ import torch  # noqa: E402
 from fp8_fine_grained_14_b300 import workloads  # noqa: E402
 
 PROFILES = os.path.join(ROOT, "profiles")
+ATTRIBUTION_IDLE_S = 0.3  # idle time before the timestamp attribution pass
 CSRC = os.path.join(ROOT, "fp8_fine_grained_14_b300", "csrc")
 
 # Dense FP8 tensor peak = measured BF16 peak x 2 (nominal dense ratio on B300:
@@ -76,7 +81,7 @@ WORKLOAD_TEXT = {
     "grouped": "grouped MoE GEMM: 8192 tokens x top-8 over 64 experts (65536 rows), X bf16 [65536,7168], "
                "W bf16 [64,2048,7168]; act + weight quant + grouped block-scaled GEMM",
     "decode": "decode-shaped skinny GEMM: X bf16 [64,7168] ~N(0,1), W [18432,7168] pre-quantised 128x128 "
-              "E4M3; act quant + block-scaled GEMM",
+              "E4M3 and pre-packed into stage images; act quant + block-scaled GEMM (packed W)",
 }
 
 
@@ -378,9 +383,14 @@ class Step:
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         self.offsets = inp["offsets"].to(device) if "offsets" in inp else None
         self.kernels = step_kernels(name)
+        self.wp = None
         if name == "decode":
+            # the weights are prepared before timing: quantised, then packed
+            # into the GEMM's stage images so each stage streams as one
+            # contiguous 16 KB copy
             with torch.cuda.stream(stream):
-                self.weight_quant()  # pre-quantised weights: outside the timed region
+                self.weight_quant()
+                self.wp = fb.fp8_pack_weight_128x128(self.qw, stream=stream)
             stream.synchronize()
 
     def _st(self):
@@ -405,6 +415,11 @@ class Step:
 
     def gemm(self):
         p = lambda t: t.data_ptr()  # noqa: E731
+        if self.wp is not None:
+            self._check("fp8_blockscaled_gemm_packed", self.lib.fp8_blockscaled_gemm_packed(
+                p(self.qa), self.qa.stride(0), p(self.sa), self.sa.stride(0), p(self.wp), p(self.sw), p(self.y),
+                self.y.stride(0), self.M, self.N, self.K, self._st()))
+            return
         self._check("fp8_blockscaled_gemm", self.lib.fp8_blockscaled_gemm(
             p(self.qa), self.qa.stride(0), p(self.sa), self.sa.stride(0), p(self.qw), self.qw.stride(0),
             p(self.sw), p(self.y), self.y.stride(0), self.M, self.N, self.K, self._st()))
@@ -415,14 +430,19 @@ class Step:
             self.G, p(self.offsets), self.M, p(self.qa), self.qa.stride(0), p(self.sa), self.sa.stride(0),
             p(self.qw), p(self.sw), p(self.y), self.y.stride(0), self.N, self.K, self._st()))
 
-    def run(self, events=None):
-        """One step; if `events` is a list, an event is recorded after each kernel."""
+    def run(self, events=None, stamps=None):
+        """One step; if `events` is a list, an event is recorded after each
+        kernel; if `stamps` is a DeviceStamps, a device timestamp is enqueued
+        after each kernel."""
         for k in self.kernels:
             getattr(self, k)()
             if events is not None:
                 ev = torch.cuda.Event(enable_timing=True)
                 ev.record(self.stream)
                 events.append(ev)
+            if stamps is not None:
+                # after the act quantiser the stamp passes on its early release
+                stamps.mark(self.stream, release_next=(k == "act_quant"))
 
     def flops(self):
         return 2 * self.M * self.N * self.K
@@ -436,6 +456,24 @@ class Step:
         if self.name == "decode":
             return gemm_bytes(M, N, K), "hbm"
         return 2 * M * N * K, "tensor"
+
+
+class DeviceStamps:
+    """Device-side timestamps (ns of the GPU's global timer) written by the
+    library's fp8bs_stream_timestamp kernel, which starts once the kernel
+    before it has completed.  Unlike an event record it keeps the step's
+    kernels programmatic dependents of one another, so the intervals between
+    consecutive stamps are each kernel's share of the step as the timed graph
+    runs it (plus about one short launch per stamp)."""
+
+    def __init__(self, fb, count, device):
+        self.fb = fb
+        self.t = torch.zeros(count, dtype=torch.int64, device=device)
+        self.i = 0
+
+    def mark(self, stream, release_next=False):
+        self.fb.fp8bs_stream_timestamp(self.t, self.i, release_next, stream)
+        self.i += 1
 
 
 def capture_steps(step, stream, steps):
@@ -504,7 +542,8 @@ def time_device(step, stream, steps, warmup, dist, device, use_graph=True):
     if status != 0:
         raise RuntimeError(f"device status word {status} after the timed region")
     del graph
-    # per-kernel attribution pass
+    # per-kernel attribution pass (stream launches: run at once, while the
+    # host is still busy, so that launches keep pace)
     events = []
     a = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -523,7 +562,54 @@ def time_device(step, stream, steps, warmup, dist, device, use_graph=True):
     status = step.fb.fp8bs_last_device_error(stream)
     if status != 0:
         raise RuntimeError(f"device status word {status} after the attribution pass")
-    return total_ms, per_kernel, sampler.summary(t0, t1, total_ms), attribution_ms, launch_mode
+    stamped = None
+    if launch_mode.startswith("CUDA graph"):
+        # one graph launch, so host speed does not matter; start it, like the
+        # timed region, from a GPU that has not just run a long burst
+        # (the power cap averages over a window)
+        time.sleep(ATTRIBUTION_IDLE_S)
+        stamped = stamp_attribution(step, stream, steps, device)
+    return total_ms, per_kernel, sampler.summary(t0, t1, total_ms), attribution_ms, launch_mode, stamped
+
+
+def stamp_attribution(step, stream, steps, device):
+    """Per-kernel shares of the step from device timestamps: the same steps
+    captured as a CUDA graph, with a timestamp kernel after every kernel (and
+    one before the first), replayed once (the stamps are device times, so
+    the graph's upload at its first launch precedes the first stamp).
+    Returns ({kernel: ms per step}, ms per step from first to last stamp,
+    SM clocks sampled during the replay), or None when the steps cannot be
+    captured."""
+    nk = len(step.kernels)
+    st = DeviceStamps(step.fb, steps * nk + 1, device)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            st.mark(stream)
+            for _ in range(steps):
+                step.run(stamps=st)
+    except Exception as e:
+        torch.cuda.synchronize()
+        print(f"note: timestamped steps could not be captured ({type(e).__name__}: {e})", file=sys.stderr)
+        return None
+    sampler = ClockSampler(device)
+    sampler.start()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(device)
+    t1 = time.perf_counter()
+    sampler.stop()
+    status = step.fb.fp8bs_last_device_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device status word {status} after the timestamp pass")
+    t = st.t.cpu().tolist()
+    del g
+    per_kernel = {k: 0.0 for k in step.kernels}
+    for i in range(steps * nk):
+        per_kernel[step.kernels[i % nk]] += (t[i + 1] - t[i]) * 1e-6
+    clocks = sampler.summary(t0, t1)
+    return {k: v / steps for k, v in per_kernel.items()}, (t[-1] - t[0]) * 1e-6 / steps, clocks
 
 
 def time_e2e(name, inp, step, stream, steps, warmup, device, fb):
@@ -958,7 +1044,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     step = Step(name, inp, device, stream, fb)
 
-    total_ms, per_kernel, clocks, attribution_ms, launch_mode = time_device(
+    total_ms, per_kernel, clocks, attribution_ms, launch_mode, stamped = time_device(
         step, stream, args.steps, args.warmup, dist, device, use_graph=not args.no_graph)
     total_ms = max_over_ranks(dist, total_ms, device)
     ms_per_step = total_ms / args.steps
@@ -977,12 +1063,16 @@ def run_ours(args):
             peak = peaks["hbm_gbs"]
             achieved = units / (ms * 1e-3) / 1e9
             unit = "GB/s"
-        kern[k] = {"us": ms * 1e3, "achieved": achieved, "unit": unit, "frac": achieved / peak, "peak": peak,
-                   "bound": bound, "algorithmic": units}
+        kern[k] = {"us_events": ms * 1e3, "achieved_events": achieved, "unit": unit, "frac_events": achieved / peak,
+                   "peak": peak, "bound": bound, "algorithmic": units}
+        if stamped is not None:
+            sms = stamped[0][k]
+            a_st = units / (sms * 1e-3) / (1e12 if bound == "tensor" else 1e9)
+            kern[k].update({"us_in_step": sms * 1e3, "achieved_in_step": a_st, "frac_in_step": a_st / peak})
     dominant = max(per_kernel, key=per_kernel.get)
     d = kern[dominant]
-    roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
-                "unit": d["unit"], "frac": d["frac"], "traffic": profiled_traffic(dominant, name),
+    roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved_events"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac_events"], "traffic": profiled_traffic(dominant, name),
                 "peak_source": (f"{peak_src} " + ("bf16 burst x 2 (dense FP8/BF16 nominal ratio)"
                                                   if d["bound"] == "tensor" else "HBM copy"))}
     if d["bound"] == "tensor":
@@ -990,12 +1080,16 @@ def run_ours(args):
         # cuBLAS figure; "frac" above keeps the stricter burst denominator
         sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
         roofline["peak_sustained"] = sustained
-        roofline["frac_of_sustained"] = d["achieved"] / sustained
+        roofline["frac_of_sustained"] = d["achieved_events"] / sustained
     nominal = NOMINAL["fp8_tflops"] if d["bound"] == "tensor" else NOMINAL["hbm_gbs"]
     roofline["peak_nominal"] = nominal
-    roofline["frac_of_nominal"] = d["achieved"] / nominal
+    roofline["frac_of_nominal"] = d["achieved_events"] / nominal
+    if "frac_in_step" in d:
+        roofline["achieved_in_step"] = d["achieved_in_step"]
+        roofline["frac_in_step"] = d["frac_in_step"]
     for k, v in kern.items():
-        v["frac_of_nominal"] = v["achieved"] / (NOMINAL["fp8_tflops"] if v["bound"] == "tensor" else NOMINAL["hbm_gbs"])
+        v["frac_of_nominal"] = v["achieved_events"] / (NOMINAL["fp8_tflops"] if v["bound"] == "tensor"
+                                                       else NOMINAL["hbm_gbs"])
 
     e2e = None
     if not args.no_e2e:
@@ -1022,9 +1116,17 @@ def run_ours(args):
                         for k, v in kern.items()},
             "tflops_gemm_only": flops / (per_kernel[step.kernels[-1]] * 1e-3) / 1e12,
             "timing": {"timed_region": f"{args.steps} steps, {launch_mode}, CUDA events on the launching stream",
-                       "kernels": f"a second pass of {args.steps} stream-launched steps with a CUDA event after "
-                                  "each kernel; a kernel's time includes the launch gap before it",
-                       "attribution_pass_ms_per_step": attribution_ms},
+                       "kernels_events": f"us_events: a second pass of {args.steps} stream-launched steps with a "
+                                         "CUDA event after each kernel; a kernel's time includes the full launch "
+                                         "gap (3-6 us) that the event record puts before it",
+                       "kernels_in_step": f"us_in_step: a third pass, the {args.steps} steps as a CUDA graph with "
+                                          "a device-timestamp kernel after each kernel; a kernel's time runs from "
+                                          "the previous kernel's end to its own, as in the timed graph, plus "
+                                          "about one short launch for the timestamp",
+                       "attribution_pass_ms_per_step": attribution_ms,
+                       "stamp_pass_ms_per_step": stamped[1] if stamped is not None else None,
+                       "stamp_pass_clocks": ({k: stamped[2].get(k) for k in ("sm_mhz", "reasons", "samples")}
+                                             if stamped is not None else None)},
             "clocks": clocks,
             "e2e": e2e,
             "gpu_launches": step_launches(step, torch.cuda.get_device_properties(device).multi_processor_count)

@@ -32,6 +32,7 @@ _API = (
     "fp8bs_last_device_error",
     "fp8bs_set_wait_timeout_ns",
     "fp8bs_selftest_wait_timeout",
+    "fp8bs_stream_timestamp",
     "linear_forward",
     "HostPipeline",
     "ld_sa_for",

@@ -56,6 +56,7 @@ EXPORTS = {
     "fp8bs_last_device_error": [_p],
     "fp8bs_set_wait_timeout_ns": [_u64],
     "fp8bs_selftest_wait_timeout": [_u64, _p],
+    "fp8bs_stream_timestamp": [_p, ctypes.c_int, _p],
 }
 for _name, _args in EXPORTS.items():
     _fn = getattr(lib, _name)
@@ -507,6 +508,17 @@ def fp8bs_set_wait_timeout_ns(ns: int):
 
 def fp8bs_selftest_wait_timeout(ns: int, stream=None):
     _check("fp8bs_selftest_wait_timeout", lib.fp8bs_selftest_wait_timeout(int(ns), _stream(stream)))
+
+
+def fp8bs_stream_timestamp(dst, index: int = 0, release_next: bool = False, stream=None):
+    """Enqueue a device timestamp (ns) into dst[index] (an int64 CUDA tensor)
+    once the work before it on the stream has completed; release_next lets
+    the next kernel launch early, as fp8_quant_act_1x128 does."""
+    if dst.dtype != torch.int64 or not dst.is_cuda or not 0 <= index < dst.numel():
+        raise ValueError("dst must be an int64 CUDA tensor and index inside it")
+    _check("fp8bs_stream_timestamp",
+           lib.fp8bs_stream_timestamp(ctypes.c_void_p(dst.data_ptr() + 8 * index), int(bool(release_next)),
+                                      _stream(stream)))
 
 
 class HostPipeline:

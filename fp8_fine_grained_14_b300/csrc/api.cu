@@ -171,7 +171,25 @@ __global__ void selftest_wait_kernel(unsigned* status, uint64_t timeout_ns) {
   }
 }
 
+// One thread: waits, as every kernel of this library does, until the grid
+// before it on the stream has completed and its writes are visible, then
+// records the device's global nanosecond timer.  Launched between two kernels
+// of a sequence, it marks where the first ended without the serialising
+// launch gap that an event record brings back.  With `release` set it lets
+// the next kernel launch before its own wait, as the kernel before it did.
+__global__ void stream_timestamp_kernel(uint64_t* dst, int release) {
+  if (release) pdl_launch_dependents();
+  pdl_wait();
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  *dst = t;
+}
+
 }  // namespace
+
+cudaError_t launch_stream_timestamp(uint64_t* dst, int release, cudaStream_t stream) {
+  return launch_pdl(stream_timestamp_kernel, dim3(1), dim3(1), 0, stream, dst, release);
+}
 
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 32, 0, stream>>>(dev.status, timeout_ns);
@@ -606,6 +624,16 @@ fp8bs_status fp8bs_last_device_error(cudaStream_t stream) {
     case fp8bs::kStatusBadOffsets: return FP8BS_ERR_INVALID_ARG;
   }
   return FP8BS_ERR_CUDA;
+}
+
+fp8bs_status fp8bs_stream_timestamp(uint64_t* dst, int release_next, cudaStream_t stream) {
+  if (dst == nullptr) return FP8BS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(dst) % 8 != 0) return FP8BS_ERR_MISALIGNED;
+  cudaError_t e;
+  const fp8bs::DeviceInfo* dev = fp8bs::current_device_info(&e);
+  if (dev == nullptr) return cuda_failure("device query", e);
+  e = fp8bs::launch_stream_timestamp(dst, release_next != 0, stream);
+  return e == cudaSuccess ? FP8BS_OK : cuda_failure("timestamp launch", e);
 }
 
 fp8bs_status fp8bs_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {

@@ -352,8 +352,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  if (!GROUPED && warp == 0 && lane == 0) {
+    // While the previous kernel of the stream finishes, pull this CTA's
+    // weight stages of its first item into L2 (dense tiles: their
+    // coordinates need no global memory); the loads after the wait then
+    // start from L2.  A prefetch changes no value read, so it is safe
+    // whatever that kernel writes.
+    TileWalker<false, BN, CG> first(p, rank);
+    int32_t a0, r0, b0, c0, g0, k0, k1, u0;
+    if (first.get(a0, r0, b0, c0, g0, k0, k1, u0)) {
+      const int32_t kend = k1 - k0 < STAGES ? k1 : k0 + STAGES;
+      for (int32_t kb = k0; kb < kend; ++kb) {
+        if (p.b_packed != nullptr && CG == 1) {
+          const uint8_t* src = p.b_packed + (static_cast<int64_t>(b0 / 128) * p.KB + kb) * kPackedTileBytes;
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            bulk_prefetch_l2(src + static_cast<int64_t>(h) * p.KB * kPackedTileBytes, kPackedTileBytes);
+        } else {
+          tma_prefetch_l2_2d(&tmB, kb * BK, b0 + rank * (BN / CG));
+        }
+      }
+    }
+  }
   // Everything above touches only this CTA's (or pair's) shared and tensor
-  // memory; from here on the kernel reads and writes global memory.
+  // memory (and L2 through hints); from here on the kernel reads and writes
+  // global memory.
   pdl_wait();
   // The pair's full and tempty barriers live in the leader.
   const uint32_t full_base = CG > 1 ? map_shared_rank(bar_full, 0) : bar_full;

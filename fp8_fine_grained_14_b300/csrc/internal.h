@@ -135,5 +135,6 @@ cudaError_t launch_swiglu_quant_act_1x128(const DeviceInfo& dev, const void* gat
                                           int64_t ldh, cudaStream_t stream);
 
 cudaError_t launch_selftest_wait(const DeviceInfo& dev, uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t launch_stream_timestamp(uint64_t* dst, int release, cudaStream_t stream);
 
 }  // namespace fp8bs

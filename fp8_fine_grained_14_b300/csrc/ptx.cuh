@@ -30,6 +30,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // order is kept in every case.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Lets the next kernel of the stream launch before this one has finished:
+// its blocks take SMs as this kernel's blocks leave them and run only what
+// precedes their own pdl_wait(), which still returns only after this whole
+// kernel has completed, so no result changes.  Worth it only before a kernel
+// that fills whole SMs (the GEMM): blocks of a small-block kernel launched
+// early pile onto the few SMs free at that moment and run there.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Record a device-side failure: first writer wins.
 __device__ __forceinline__ void record_status(unsigned* status, unsigned code) {
   atomicCAS(status, 0u, code);
@@ -122,6 +132,21 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Hints that pull global memory into L2 and nothing else: they change no
+// value any thread reads, so they may run before pdl_wait().
+// A 2-D tile of `map` at (x, y), the box a tma_load_2d of the same map copies.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+// `bytes` contiguous bytes at `src` (both multiples of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // 2-D tile load global -> shared; completion counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x, int32_t y) {
   asm volatile(

@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(256, 6) quant_act_1x128_kernel(const uint4* __
                                                               int64_t ldx_v, uint4* __restrict__ q, int64_t ldq_v,
                                                               float* __restrict__ sa, int64_t ld_sa) {
   pdl_wait();
+  // The codes usually feed the GEMM next: let it set up (and pull its first
+  // weight stages into L2) while this kernel finishes.
+  pdl_launch_dependents();
   const int lane8 = threadIdx.x & 7;
   const int r = threadIdx.x >> 3;  // 32 rows per CTA
   const int64_t kb0 = static_cast<int64_t>(blockIdx.x) * U;

@@ -412,6 +412,23 @@ void fp8bs_set_wait_timeout_ns(uint64_t timeout_ns);
  */
 fp8bs_status fp8bs_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
+/*
+ * Measurement aid, no counterpart in the method.  Enqueues on `stream` a
+ * one-thread kernel that waits until the work before it on the stream has
+ * completed, then writes the device's global timer (nanoseconds) to *dst
+ * (device memory, 8-byte aligned, owned by the caller).  The library's
+ * kernels launch as programmatic dependents of the work before them, and
+ * fp8_quant_act_1x128 lets the next kernel launch before it finishes, so
+ * that a GEMM after it sets up early; release_next != 0 makes the timestamp
+ * do the same (pass it for a timestamp placed right after that call).
+ * Placed between kernels this way, consecutive timestamps split a sequence
+ * into per-kernel intervals (each including the short dependent-launch gap
+ * before its kernel) without the full launch gap that a recorded event adds.
+ * Returns FP8BS_ERR_INVALID_ARG for a null dst, FP8BS_ERR_MISALIGNED for an
+ * unaligned one.
+ */
+fp8bs_status fp8bs_stream_timestamp(uint64_t* dst, int release_next, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -200,6 +200,14 @@ def test_gemm_packed_validation(lib, args, expect):
     assert lib.fp8_blockscaled_gemm_packed(*args) == expect
 
 
+@pytest.mark.parametrize("args,expect", [
+    ((None, 0, None), 1),        # null destination
+    ((P(0x10004), 1, None), 2),  # not 8-byte aligned
+])
+def test_stream_timestamp_validation(lib, args, expect):
+    assert lib.fp8bs_stream_timestamp(*args) == expect
+
+
 def test_header_is_plain_c(tmp_path):
     """include/fp8bs.h compiles as C (no C++ in the ABI)."""
     import shutil

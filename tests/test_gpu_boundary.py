@@ -68,6 +68,31 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert fb.fp8bs_last_device_error() == 0
 
 
+def test_stream_timestamps_bracket_a_kernel():
+    """Timestamps before and after a GEMM are ordered and span the kernel:
+    the interval is positive and no longer than the host-observed wall time
+    of the whole enqueue-and-synchronise."""
+    import time
+
+    x, w = workloads.dense_inputs(2048, 4096, 4096, seed=5)
+    xd, wd = x.to(DEV), w.to(DEV)
+    qa, sa = fb.fp8_quant_act_1x128(xd)
+    qw, sw = fb.fp8_quant_weight_128x128(wd)
+    t = torch.zeros(3, dtype=torch.int64, device=DEV)
+    torch.cuda.synchronize()
+    h0 = time.perf_counter_ns()
+    fb.fp8bs_stream_timestamp(t, 0)
+    fb.fp8_blockscaled_gemm(qa, sa, qw, sw)
+    fb.fp8bs_stream_timestamp(t, 1)
+    fb.fp8bs_stream_timestamp(t, 2)
+    torch.cuda.synchronize()
+    h1 = time.perf_counter_ns()
+    t0, t1, t2 = t.tolist()
+    assert 0 < t0 < t1 <= t2
+    assert t1 - t0 < h1 - h0
+    assert fb.fp8bs_last_device_error() == 0
+
+
 def test_gemm_repeatable():
     """Two launches on the same inputs give bit-identical outputs."""
     x, w = workloads.dense_inputs(700, 1024, 1024, seed=8)

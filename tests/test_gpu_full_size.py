@@ -13,7 +13,8 @@ Method: "The Definitive Information To Deepseek" -- 1x128 activation tiles and
 must satisfy |y_gpu - y_ref| <= 1e-2 |y_ref| + 1e-3 rms(y_ref), with rms over
 the whole output of the workload (for the grouped GEMM, the concatenated
 sum(m_g) x N output).  The GPU runs each workload through the same entry
-points, shapes and strides as the benchmark's timed step.
+points, shapes and strides as the benchmark's timed step (the decode GEMM
+both on plain and on packed weights).
 """
 import numpy as np
 import pytest
@@ -49,6 +50,10 @@ def _check_quant(pool, x, w2d, qa, sa, qw2d, sw2d, what):
 def test_dense_full_size(pool, name):
     x, w = workloads.config_inputs(name)
     y, (qa, sa, qw, sw) = fb.linear_forward(x.to(DEV), w.to(DEV))
+    y_packed = None
+    if name == "decode":
+        # the decode step streams weights packed before timing
+        y_packed = fb.fp8_blockscaled_gemm_packed(qa, sa, fb.fp8_pack_weight_128x128(qw), sw).cpu()
     torch.cuda.synchronize()
     assert fb.fp8bs_last_device_error() == 0
     y = y.cpu()
@@ -56,6 +61,9 @@ def test_dense_full_size(pool, name):
     del qa, sa, qw, sw
     y_ref = pool.blockscaled_gemm(qa_r, sa_r, qw_r, sw_r)
     assert_gemm_close_rows(y, y_ref, what=name)
+    if y_packed is not None:
+        assert_gemm_close_rows(y_packed, y_ref, what=name + " (packed W)")
+        assert torch.equal(y_packed, y), "packed-weight GEMM differs from the plain one"
 
 
 def test_grouped_full_size(pool):
