@@ -91,9 +91,9 @@ WORKLOAD_TEXT = {
 # ---------------------------------------------------------------------------
 def step_launches(step, num_sms):
     """Kernel launches of one step: one per kernel of the step, and the dense
-    GEMM's split-K reduction when it runs."""
+    GEMM's split-K reduction when it runs (not on packed weights)."""
     n = len(step.kernels)
-    if step.kernels[-1] == "gemm":
+    if step.kernels[-1] == "gemm" and step.wp is None:
         n += gemm_kernel_launches(step.M, step.N, step.K, num_sms) - 1
     return n
 

@@ -33,6 +33,11 @@ def _grouped_gpu(offsets, x, w):
     ([0, 0, 1], 384, 128),
     ([500], 512, 256),
     ([77, 300, 0, 129, 5, 64, 200, 1], 1024, 512),  # 256-wide tiles across ragged groups
+    # 256-wide pair tiles: these counts put 0, 1, 127, 128, 129, 255 and 256
+    # rows after a group's whole 256-row tiles (one or both CTAs of its last
+    # pair masked), first and last groups included
+    ([1, 256, 257, 384, 385, 128, 0, 129, 511, 640, 127, 768], 512, 384),
+    ([0, 0, 300], 256, 256),
 ])
 def test_grouped_small(counts, N, K):
     G = len(counts)
