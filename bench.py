@@ -816,31 +816,48 @@ _FLUSH = None
 
 
 def _time_kernel(fn, iters=40, warmup=3):
-    """Median CUDA-event time (ms) of fn() on the current stream.  Between
-    iterations a 512 MB buffer is read (a sum), which evicts every input from
-    L2 without leaving dirty lines whose write-back would be charged to the
-    timed kernel."""
+    """Time of fn() on the current stream, L2 evicted before each of `iters`
+    runs: a 512 MB buffer is read (a sum), which evicts every input from L2
+    without leaving dirty lines whose write-back would be charged to the
+    timed call.  Returns (ms from device timestamps, ms from CUDA events),
+    each the mean of the middle half of the runs.  The timestamps are
+    fp8bs_stream_timestamp kernels before and after the call; the library's
+    kernels launch as programmatic dependents of the first, so the interval
+    is the call's kernels plus one short dependent-launch gap.  Event
+    timestamps advance in steps of about 2 us here and each event interval
+    also holds the full launch gap before the kernel.  Output lines still
+    dirty in L2 when the call ends are written back during the next eviction
+    read, so a row that writes much (E5M6: as many bytes as it reads) can
+    read above the copy peak."""
     global _FLUSH
     if _FLUSH is None:
         _FLUSH = torch.ones(128 * 2 ** 20, dtype=torch.float32, device="cuda")
+    fb = load_library()
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    stamps = torch.zeros(2 * iters, dtype=torch.int64, device="cuda")
     ts = []
-    for _ in range(iters):
+    for i in range(iters):
         _FLUSH.sum()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
+        fb.fp8bs_stream_timestamp(stamps, 2 * i)
         fn()
+        fb.fp8bs_stream_timestamp(stamps, 2 * i + 1)
         b.record()
         b.synchronize()
         ts.append(a.elapsed_time(b))
-    # event timestamps are coarse (a few microseconds apart for short kernels):
-    # average the middle half instead of taking a median
-    ts.sort()
-    mid = ts[len(ts) // 4: len(ts) - len(ts) // 4]
-    return sum(mid) / len(mid)
+    t = stamps.cpu().tolist()
+    ds = [(t[2 * i + 1] - t[2 * i]) * 1e-6 for i in range(iters)]
+
+    def middle_mean(v):
+        v = sorted(v)
+        mid = v[len(v) // 4: len(v) - len(v) // 4]
+        return sum(mid) / len(mid)
+
+    return middle_mean(ds), middle_mean(ts)
 
 
 def _time_cpu(fn, budget_s=2.0):
@@ -874,17 +891,24 @@ def run_rows(args):
         return (torch.randn(*shape, generator=gc) * std).to(torch.bfloat16).float().numpy()
 
     lines = []
+    sampler = ClockSampler(dev, period_s=0.001)
+    sampler.start()
 
     def emit(row, what, timer, work, unit, oracle_fn=None, oracle_work=None, oracle_sample=""):
         if args.only and not any(t in f"{row} {what}" for t in args.only.split("|")):
             return
-        ms = timer()
-        if unit == "GB/s":
-            achieved, peak = work / (ms * 1e-3) / 1e9, peaks["hbm_gbs"]
-        else:
-            achieved, peak = work / (ms * 1e-3) / 1e12, fp8_peak
+        t0 = time.perf_counter()
+        ms, ms_events = timer()
+        clocks = sampler.summary(t0, time.perf_counter())
+        scale = 1e9 if unit == "GB/s" else 1e12
+        peak = peaks["hbm_gbs"] if unit == "GB/s" else fp8_peak
+        achieved = work / (ms * 1e-3) / scale
         line = {"row": row, "workload": what, "us": ms * 1e3, "achieved": achieved, "unit": unit, "peak": peak,
-                "frac": achieved / peak, "peak_source": peak_src, "algorithmic": work}
+                "frac": achieved / peak, "us_events": ms_events * 1e3,
+                "frac_events": work / (ms_events * 1e-3) / scale / peak, "peak_source": peak_src,
+                "algorithmic": work,
+                "timing": "device timestamps around the call (L2 evicted before each run); us_events: CUDA events",
+                "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_mhz_min", "reasons", "samples")}}
         if oracle_fn is not None and not args.no_cpu_baseline:
             t = _time_cpu(oracle_fn)
             scale = 1e9 if unit == "GB/s" else 1e12
@@ -1012,6 +1036,7 @@ def run_rows(args):
          lambda: _time_kernel(lambda: fb.fp8_swiglu_quant_act_1x128(gu, qa=qh, sa=sh)),
          4 * M * F + M * F + 4 * M * (F // 128), "GB/s", lambda: oracle.swiglu_quant_act_1x128(gus),
          5 * 128 * F, "rows[:128]")
+    sampler.stop()
     return lines
 
 

@@ -151,6 +151,25 @@ __device__ __forceinline__ uint32_t fix_word_cols(uint32_t code, uint32_t specia
   return code;
 }
 
+// quantise8_cols with the per-column constants already paired as the packed
+// arithmetic takes them: r2[i] = (r of column 2i, r of column 2i + 1), and
+// likewise sn2 for -s (pairs built once per thread, not once per vector).
+__device__ __forceinline__ uint2 quantise8_cols_paired(const uint4 v, const float2 (&r2)[4], const float2 (&sn2)[4],
+                                                       const GroupScale (&g)[8], uint32_t special0,
+                                                       uint32_t special1) {
+  const float2 a = quotient2(bf16x2_to_f32x2(v.x), r2[0], sn2[0]);
+  const float2 b = quotient2(bf16x2_to_f32x2(v.y), r2[1], sn2[1]);
+  const float2 c = quotient2(bf16x2_to_f32x2(v.z), r2[2], sn2[2]);
+  const float2 d = quotient2(bf16x2_to_f32x2(v.w), r2[3], sn2[3]);
+  uint32_t lo = cvt_e4m3x4(a.x, a.y, b.x, b.y) | sign_bytes(v.x, v.y);
+  uint32_t hi = cvt_e4m3x4(c.x, c.y, d.x, d.y) | sign_bytes(v.z, v.w);
+  if ((special0 | special1) != 0u) {
+    lo = fix_word_cols(lo, special0, v.x, v.y, g[0].s, g[1].s, g[2].s, g[3].s);
+    hi = fix_word_cols(hi, special1, v.z, v.w, g[4].s, g[5].s, g[6].s, g[7].s);
+  }
+  return make_uint2(lo, hi);
+}
+
 __device__ __forceinline__ uint2 quantise8_cols(const uint4 v, const GroupScale (&g)[8], uint32_t special0,
                                                 uint32_t special1) {
   const float2 a = quotient2(bf16x2_to_f32x2(v.x), make_float2(g[0].r.x, g[1].r.x),

@@ -58,91 +58,29 @@ __global__ void __launch_bounds__(256) quant_per_token_kernel(const uint4* __res
 }
 
 // ---------------------------------------------------------------------------
-// Per channel, two passes (inputs taller than the one-pass cluster kernel
-// below takes): (1) column maxima of |x| as BF16 bit patterns (non-negative
-// values order like their patterns), reduced across a CTA in shared memory
-// and merged into s with atomicMax, (2) every element quantised with its
-// column's scale, (3) s turned from maxima into scales.  A CTA covers 256
-// columns (thread t: the 8 columns of vector t % 32) and walks row tiles of 64
-// (thread t: rows t / 32 + 8 i).
+// Per channel: a cluster of kPcCluster CTAs covers a strip of SV vectors of 8
+// channels and all M rows, CTA rank r the r-th of kPcCluster equal row
+// ranges.  Thread t takes vector t % SV of the strip and rows t / SV +
+// (T / SV) i of its range, so a warp reads 32 / SV rows of 16 SV contiguous
+// bytes per instruction.  Pass 1 streams those rows for the column maxima of
+// |x| (BF16 bit patterns: non-negative values order like their patterns),
+// combined across the warp's row phases (shuffles), the CTA's warps (shared
+// memory) and the cluster (each CTA reads every rank's maxima through
+// distributed shared memory).  Pass 2 reads the same rows again and codes
+// them: all of X was read a moment before (with an evict-last L2 policy), so
+// while X fits in L2 (58.7 MB for 4096 x 7168 against 126 MB) the second
+// read comes from L2 and HBM sees X once.  Nothing stays in registers between
+// the passes.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) channel_absmax_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
-                                                             int64_t ldx_v, uint32_t* __restrict__ amax_bits) {
-  pdl_wait();
-  __shared__ uint32_t part[8][32 * 4];  // [row slot][packed column pairs]
-  const int lane = threadIdx.x & 31, r8 = threadIdx.x >> 5;
-  const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
-  const int64_t row_tiles = (M + 63) / 64;
-  uint32_t mm[4] = {0u, 0u, 0u, 0u};
-  if (col_v < KV) {
-    for (int64_t tile = blockIdx.y; tile < row_tiles; tile += gridDim.y) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int64_t row = tile * 64 + r8 + 8 * i;
-        if (row < M) {
-          const uint4 v = ld_nc_v4(x + row * ldx_v + col_v);
-          constexpr uint32_t kMag = 0x7FFF7FFFu;
-          mm[0] = max_pairs(mm[0], v.x & kMag);
-          mm[1] = max_pairs(mm[1], v.y & kMag);
-          mm[2] = max_pairs(mm[2], v.z & kMag);
-          mm[3] = max_pairs(mm[3], v.w & kMag);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) part[r8][lane * 4 + i] = mm[i];
-  __syncthreads();
-  if (r8 == 0 && col_v < KV) {
-    uint32_t* dst = amax_bits + col_v * 8;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t m = part[0][lane * 4 + i];
-#pragma unroll
-      for (int k = 1; k < 8; ++k) m = max_pairs(m, part[k][lane * 4 + i]);
-      atomicMax(dst + 2 * i, m & 0xFFFFu);
-      atomicMax(dst + 2 * i + 1, m >> 16);
-    }
-  }
-}
-
-__global__ void __launch_bounds__(256) quant_per_channel_kernel(const uint4* __restrict__ x, int64_t M, int64_t KV,
-                                                                int64_t ldx_v, const uint32_t* __restrict__ amax_bits,
-                                                                uint2* __restrict__ q, int64_t ldq_v) {
-  pdl_wait();
-  const int lane = threadIdx.x & 31, r8 = threadIdx.x >> 5;
-  const int64_t col_v = static_cast<int64_t>(blockIdx.x) * 32 + lane;
-  if (col_v >= KV) return;
-  GroupScale g[8];  // the scales of this thread's 8 columns
-  uint32_t special0 = 0u, special1 = 0u;  // zero scales or scales below 2^-64, 0xFF per element
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    g[c] = group_scale(__uint_as_float(__ldg(amax_bits + col_v * 8 + c) << 16));
-    const uint32_t mark = (g[c].s == 0.0f || !g[c].fast) ? 0xFFu : 0u;
-    if (c < 4)
-      special0 |= mark << (8 * c);
-    else
-      special1 |= mark << (8 * (c - 4));
-  }
-  const int64_t row_tiles = (M + 63) / 64;
-  for (int64_t tile = blockIdx.y; tile < row_tiles; tile += gridDim.y) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int64_t row = tile * 64 + r8 + 8 * i;
-      if (row < M) q[row * ldq_v + col_v] = quantise8_cols(ld_nc_v4(x + row * ldx_v + col_v), g, special0, special1);
-    }
-  }
-}
-
-// Per channel in one pass, for M <= kPcCluster * 32 * 16 rows: a cluster of
-// kPcCluster CTAs covers 64 channels and all rows (CTA rank r: rows 32 R r ..
-// 32 R r + 32 R - 1), each thread holding R 16-byte vectors (8 channels of R
-// rows, row phase t / 8) in registers.  Column maxima combine per thread,
-// across the warp's four row phases (shuffles), across the eight warps
-// (shared memory) and across the cluster (each CTA reads every rank's maxima
-// through distributed shared memory after a cluster barrier); then every CTA
-// codes its rows from registers, so X is read once and no atomics are needed.
 constexpr int kPcCluster = 8;
+// 8 vectors (64 channels, 128 bytes of a row) per strip and 128-thread CTAs:
+// seven CTAs per SM, so a 4096 x 7168 input's 896 CTAs run in one wave.
+// (Strips of 16 or 32 vectors, with fewer, larger CTAs, measured slower.)
+constexpr int kPcSV = 8;           // vectors (of 8 channels) per strip
+constexpr int kPcThreads = 128;    // threads per CTA
+constexpr int kPcMinBlocks = 7;    // CTAs per SM (72 registers a thread)
+constexpr int kPcUnroll = 8;       // loads in flight per thread
+static_assert(kPcSV <= 32 && 32 % kPcSV == 0 && kPcThreads % 32 == 0, "strip layout");
 
 __device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
   uint4 v;
@@ -153,55 +91,77 @@ __device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
   return v;
 }
 
-template <int R>
-__global__ void __launch_bounds__(256) quant_per_channel_cluster_kernel(const uint4* __restrict__ x, int64_t M,
-                                                                        int64_t KV, int64_t ldx_v,
-                                                                        uint2* __restrict__ q, int64_t ldq_v,
-                                                                        float* __restrict__ s) {
+template <int SV, int T>
+__global__ void __launch_bounds__(T, kPcMinBlocks) quant_per_channel_kernel(const uint4* __restrict__ x, int64_t M,
+                                                                     int64_t KV, int64_t ldx_v,
+                                                                     int64_t rows_per_cta, uint2* __restrict__ q,
+                                                                     int64_t ldq_v, float* __restrict__ s) {
+  constexpr int kWarps = T / 32;
+  constexpr int kPhases = T / SV;  // row phases of a CTA
+  constexpr int kStep = kPhases * kPcUnroll;
   pdl_wait();
-  __shared__ uint32_t warp_max[8][8][4];            // [warp][channel group][BF16 pair]
-  __shared__ __align__(16) uint32_t cta_max[8][4];  // [channel group][BF16 pair]: this CTA's maxima
+  __shared__ uint32_t warp_max[kWarps][SV][4];       // [warp][vector][BF16 pair]
+  __shared__ __align__(16) uint32_t cta_max[SV][4];  // [vector][BF16 pair]: this CTA's maxima
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int cg = t & 7, rp = t >> 3;
+  const int cg = t % SV, rp = t / SV;
   const uint32_t rank = cluster_ctarank();
-  const int64_t cb = blockIdx.x / kPcCluster;
-  const int64_t col_v = cb * 8 + cg;
+  const int64_t col_v = static_cast<int64_t>(blockIdx.x / kPcCluster) * SV + cg;
   const bool col_ok = col_v < KV;
-  const int64_t row0 = static_cast<int64_t>(rank) * (32 * R) + rp;
-  uint4 v[R];
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int64_t row = row0 + 32 * i;
-    v[i] = (col_ok && row < M) ? ld_nc_v4(x + row * ldx_v + col_v) : make_uint4(0u, 0u, 0u, 0u);
-  }
+  const int64_t r_begin = static_cast<int64_t>(rank) * rows_per_cta;
+  const int64_t r_end = r_begin + rows_per_cta < M ? r_begin + rows_per_cta : M;
+  const uint4* xc = x + col_v;
   constexpr uint32_t kMag = 0x7FFF7FFFu;
+
+  // pass 1: column maxima of this CTA's rows, which stay in L2 for pass 2
+  // (evict-last; pass 2 reads them evict-first and stores the codes so)
+  const uint64_t keep = l2_evict_last_policy(), drop = l2_evict_first_policy();
   uint32_t m0 = 0u, m1 = 0u, m2 = 0u, m3 = 0u;
+  if (col_ok) {
+    const uint4* xp = xc + (r_begin + rp) * ldx_v;
+    const int64_t xstep = kPhases * ldx_v;
+    int64_t r = r_begin + rp;
+    for (; r + kPhases * (kPcUnroll - 1) < r_end; r += kStep) {
+      uint4 v[kPcUnroll];
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    m0 = max_pairs(m0, v[i].x & kMag);
-    m1 = max_pairs(m1, v[i].y & kMag);
-    m2 = max_pairs(m2, v[i].z & kMag);
-    m3 = max_pairs(m3, v[i].w & kMag);
+      for (int i = 0; i < kPcUnroll; ++i) v[i] = ld_nc_v4_hint(xp + i * xstep, keep);
+#pragma unroll
+      for (int i = 0; i < kPcUnroll; ++i) {
+        m0 = max_pairs(m0, v[i].x & kMag);
+        m1 = max_pairs(m1, v[i].y & kMag);
+        m2 = max_pairs(m2, v[i].z & kMag);
+        m3 = max_pairs(m3, v[i].w & kMag);
+      }
+      xp += kPcUnroll * xstep;
+    }
+    for (; r < r_end; r += kPhases) {
+      const uint4 v = ld_nc_v4_hint(xp, keep);
+      m0 = max_pairs(m0, v.x & kMag);
+      m1 = max_pairs(m1, v.y & kMag);
+      m2 = max_pairs(m2, v.z & kMag);
+      m3 = max_pairs(m3, v.w & kMag);
+      xp += xstep;
+    }
   }
+  // lanes SV p + cg of a warp hold the same vector for its row phases p
 #pragma unroll
-  for (int off = 8; off <= 16; off <<= 1) {
+  for (int off = SV; off < 32; off <<= 1) {
     m0 = max_pairs(m0, __shfl_xor_sync(0xffffffffu, m0, off));
     m1 = max_pairs(m1, __shfl_xor_sync(0xffffffffu, m1, off));
     m2 = max_pairs(m2, __shfl_xor_sync(0xffffffffu, m2, off));
     m3 = max_pairs(m3, __shfl_xor_sync(0xffffffffu, m3, off));
   }
-  if (lane < 8) {
+  if (lane < SV) {
     warp_max[warp][lane][0] = m0;
     warp_max[warp][lane][1] = m1;
     warp_max[warp][lane][2] = m2;
     warp_max[warp][lane][3] = m3;
   }
   __syncthreads();
-  if (t < 32) {
+  if (t < 4 * SV) {
     const int c = t >> 2, w = t & 3;
     uint32_t mm = warp_max[0][c][w];
 #pragma unroll
-    for (int k = 1; k < 8; ++k) mm = max_pairs(mm, warp_max[k][c][w]);
+    for (int k = 1; k < kWarps; ++k) mm = max_pairs(mm, warp_max[k][c][w]);
     cta_max[c][w] = mm;
   }
   cluster_sync_all();  // every CTA's maxima visible to the cluster
@@ -228,32 +188,38 @@ __global__ void __launch_bounds__(256) quant_per_channel_cluster_kernel(const ui
     else
       special1 |= mark << (8 * (c - 4));
   }
-  if (col_ok) {
+  if (!col_ok) return;
+  if (rank == 0 && rp == 0) {
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int64_t row = row0 + 32 * i;
-      if (row < M) q[row * ldq_v + col_v] = quantise8_cols(v[i], g, special0, special1);
-    }
-    if (rank == 0 && rp == 0) {
+    for (int c = 0; c < 8; ++c) s[col_v * 8 + c] = g[c].s;
+  }
+  float2 r2[4], sn2[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) s[col_v * 8 + c] = g[c].s;
-    }
+  for (int i = 0; i < 4; ++i) {
+    r2[i] = make_float2(g[2 * i].r.x, g[2 * i + 1].r.x);
+    sn2[i] = make_float2(g[2 * i].s_neg.x, g[2 * i + 1].s_neg.x);
   }
-}
-
-__global__ void channel_scales_kernel(uint32_t* __restrict__ amax_bits_to_scales, int64_t K) {
-  pdl_wait();
-  const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (k < K) {
-    const float amax = __uint_as_float(amax_bits_to_scales[k] << 16);
-    amax_bits_to_scales[k] = __float_as_uint(group_scale(amax).s);
+  // pass 2: the same rows again (from L2 while X fits there), coded; whole
+  // groups of kPcUnroll rows without per-row checks, then the ragged rest
+  const uint4* xp = xc + (r_begin + rp) * ldx_v;
+  uint2* qp = q + (r_begin + rp) * ldq_v + col_v;
+  const int64_t xstep = kPhases * ldx_v, qstep = kPhases * ldq_v;
+  int64_t r = r_begin + rp;
+  for (; r + kPhases * (kPcUnroll - 1) < r_end; r += kStep) {
+    uint4 v[kPcUnroll];
+#pragma unroll
+    for (int i = 0; i < kPcUnroll; ++i) v[i] = ld_nc_v4_hint(xp + i * xstep, drop);
+#pragma unroll
+    for (int i = 0; i < kPcUnroll; ++i)
+      st_global_v2_hint(qp + i * qstep, quantise8_cols_paired(v[i], r2, sn2, g, special0, special1), drop);
+    xp += kPcUnroll * xstep;
+    qp += kPcUnroll * qstep;
   }
-}
-
-__global__ void zero_words_kernel(uint32_t* __restrict__ p, int64_t n) {
-  pdl_wait();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0u;
+  for (; r < r_end; r += kPhases) {
+    st_global_v2_hint(qp, quantise8_cols_paired(ld_nc_v4_hint(xp, drop), r2, sn2, g, special0, special1), drop);
+    xp += xstep;
+    qp += qstep;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -456,9 +422,13 @@ if (KV <= 256)
   return cudaGetLastError();
 }
 
-template <int R>
-cudaError_t launch_per_channel_cluster(const void* x, int64_t M, int64_t KV, int64_t ldx, void* q, int64_t ldq,
-                                       float* s, cudaStream_t stream) {
+cudaError_t launch_quant_per_channel(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     void* q, int64_t ldq, float* s, cudaStream_t stream) {
+  (void)dev;
+  const int64_t KV = K / 8;
+  constexpr int kPhases = kPcThreads / kPcSV;
+  int64_t rows_per_cta = (M + kPcCluster - 1) / kPcCluster;
+  rows_per_cta = (rows_per_cta + kPhases - 1) / kPhases * kPhases;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = kPcCluster;
@@ -467,43 +437,15 @@ cudaError_t launch_per_channel_cluster(const void* x, int64_t M, int64_t KV, int
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((KV + 7) / 8 * kPcCluster), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>((KV + kPcSV - 1) / kPcSV * kPcCluster), 1, 1);
+  cfg.blockDim = dim3(kPcThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, quant_per_channel_cluster_kernel<R>, static_cast<const uint4*>(x), M, KV, ldx / 8,
-                            static_cast<uint2*>(q), ldq / 8, s);
-}
-
-cudaError_t launch_quant_per_channel(const DeviceInfo& dev, const void* x, int64_t M, int64_t K, int64_t ldx,
-                                     void* q, int64_t ldq, float* s, cudaStream_t stream) {
-  (void)dev;
-  const int64_t KV = K / 8;
-  // One pass on clusters when every row fits a cluster's registers.
-  cudaError_t e = cudaErrorNotSupported;
-  if (M <= kPcCluster * 32 * 1)
-    e = launch_per_channel_cluster<1>(x, M, KV, ldx, q, ldq, s, stream);
-  else if (M <= kPcCluster * 32 * 2)
-    e = launch_per_channel_cluster<2>(x, M, KV, ldx, q, ldq, s, stream);
-  else if (M <= kPcCluster * 32 * 4)
-    e = launch_per_channel_cluster<4>(x, M, KV, ldx, q, ldq, s, stream);
-  else if (M <= kPcCluster * 32 * 8)
-    e = launch_per_channel_cluster<8>(x, M, KV, ldx, q, ldq, s, stream);
-  else if (M <= kPcCluster * 32 * 16)
-    e = launch_per_channel_cluster<16>(x, M, KV, ldx, q, ldq, s, stream);
-  if (e != cudaErrorNotSupported) return e == cudaSuccess ? cudaGetLastError() : e;
-  uint32_t* bits = reinterpret_cast<uint32_t*>(s);
-  (void)launch_pdl(zero_words_kernel, static_cast<unsigned>((K + 255) / 256), 256, 0, stream, bits, K);
-  const int64_t row_tiles = (M + 63) / 64;
-  const dim3 grid(static_cast<unsigned>((KV + 31) / 32),
-                  static_cast<unsigned>(row_tiles < kMaxGridY ? row_tiles : kMaxGridY));
-  (void)launch_pdl(channel_absmax_kernel, grid, 256, 0, stream, static_cast<const uint4*>(x), M, KV, ldx / 8, bits);
-  (void)launch_pdl(quant_per_channel_kernel, grid, 256, 0, stream, static_cast<const uint4*>(x), M, KV, ldx / 8, bits,
-                                                     static_cast<uint2*>(q), ldq / 8);
-  (void)launch_pdl(channel_scales_kernel, static_cast<unsigned>((K + 255) / 256), 256, 0, stream, bits, K);
-  return cudaGetLastError();
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, quant_per_channel_kernel<kPcSV, kPcThreads>, static_cast<const uint4*>(x), M, KV,
+                                           ldx / 8, rows_per_cta, static_cast<uint2*>(q), ldq / 8, s);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_cast_e5m6(const DeviceInfo& dev, const void* x, int64_t n, void* codes, cudaStream_t stream) {

@@ -289,8 +289,8 @@ fp8bs_status fp8_quant_per_token(const void* x_bf16, int64_t M, int64_t K, int64
 /*
  * Per channel: one scale per column of X [M, K] BF16 over all M rows.
  *   q : [M, K] codes (row stride ldq);  s : [K] FP32 scales, contiguous,
- *   16-byte aligned (used as the column-maximum accumulator while the call
- *   runs).  K % 8 == 0.  X is read twice (maxima, then codes).
+ *   16-byte aligned.  K % 8 == 0.  X is read twice (maxima, then codes), in
+ *   one kernel; while X fits in L2 the second read is served from there.
  */
 fp8bs_status fp8_quant_per_channel(const void* x_bf16, int64_t M, int64_t K, int64_t ldx, void* q, int64_t ldq,
                                    float* s, cudaStream_t stream);

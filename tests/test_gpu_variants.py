@@ -47,9 +47,9 @@ def test_per_token(M, K):
 @pytest.mark.parametrize("M,K", [(1, 16), (130, 144), (300, 2048), (257, 528), (2048, 144), (2049, 16),
                                  (3000, 144), (2500, 1552), (4096, 64), (4096, 7168), (4097, 144), (6000, 256)])
 def test_per_channel(M, K):
-    """Up to 4096 rows: the one-pass cluster kernel, at every row count per
-    thread (ragged rows, a single and a ragged last 64-channel group
-    included); beyond: the two-pass kernels."""
+    """The cluster kernel (8 CTAs share a 64-channel strip's rows): ragged
+    row ranges, CTAs with no rows (M < 8 x 16), a single and a ragged last
+    64-channel group, and inputs taller than 4096 rows."""
     x = _edge_matrix(M, K, seed=3 * M + K)
     q, s = fb.fp8_quant_per_channel(x.to(DEV))
     torch.cuda.synchronize()
