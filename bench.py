@@ -28,7 +28,9 @@ the workload per step, on this host's cores (rank 0 only).
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 torch.cuda.synchronize(), timed by CUDA events on the launching stream; the
 maximum over ranks is reported.  The K steps are replayed from a CUDA graph
-of their C-ABI calls (--no-graph: stream launches).  Per-kernel times come
+of their C-ABI calls (--no-graph: stream launches); a short device-side busy
+wait before the start event covers the host's launch of the region, so the
+events time the K steps alone.  Per-kernel times come
 from two more passes: K stream-launched steps with a CUDA event after every
 kernel (us_events: each includes the full launch gap that the event puts
 before its kernel), and the K steps as a graph with a device-timestamp kernel
@@ -60,6 +62,7 @@ from fp8_fine_grained_14_b300 import workloads  # noqa: E402
 
 PROFILES = os.path.join(ROOT, "profiles")
 ATTRIBUTION_IDLE_S = 0.3  # idle time before the timestamp attribution pass
+HOLD_BEFORE_REGION_US = 500  # device busy wait that covers the host's launch of the timed region
 CSRC = os.path.join(ROOT, "fp8_fine_grained_14_b300", "csrc")
 
 # Dense FP8 tensor peak = measured BF16 peak x 2 (nominal dense ratio on B300:
@@ -476,6 +479,14 @@ class DeviceStamps:
         self.i += 1
 
 
+def hold_gpu(stream, us):
+    """Enqueue a device-side busy wait of about `us` microseconds."""
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None and us > 0:
+        with torch.cuda.stream(stream):
+            sleep(int(us * 2000))  # cycles at about 2 GHz
+
+
 def capture_steps(step, stream, steps):
     """The C-ABI calls of `steps` steps recorded into one CUDA graph (the
     kernels, their arguments and their order; the library's host-side
@@ -526,6 +537,10 @@ def time_device(step, stream, steps, warmup, dist, device, use_graph=True):
     end = torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
+        # keep the GPU busy (a device-side sleep, outside the timed window)
+        # while the host enqueues the start event and the graph launch, so
+        # the window holds the K steps and none of the host's launch time
+        hold_gpu(stream, HOLD_BEFORE_REGION_US)
         start.record(stream)
         if graph is not None:
             graph.replay()
