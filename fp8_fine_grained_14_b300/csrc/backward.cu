@@ -176,35 +176,47 @@ __global__ void __launch_bounds__(256, TQuant<FROM_FP8>::kCtasPerSm) quant_act_1
 // 128x128 code blocks of W [N, K] -> W^T [K, N], and the block-scale matrix
 // transposed.  One CTA per block, N blocks fastest in the grid (concurrent
 // CTAs then write adjacent 128-byte pieces of the same W^T rows, which
-// measured faster than reading adjacent pieces of the same W rows): 16-byte
-// loads into shared memory, then
-// thread t takes the input columns 4 (t % 32) .. + 3 over the 16 rows
-// 16 (t / 32) .., reading 4x4 byte squares with 32-bit loads and transposing
-// them with byte permutes; each of its 4 output rows leaves as one 16-byte run.
+// measured faster than reading adjacent pieces of the same W rows): the block
+// arrives in shared memory by one TMA copy, then thread t takes the input
+// columns 4 (t % 32) .. + 3 over the 16 rows 16 (t / 32) .., reading 4x4 byte
+// squares with 32-bit loads and transposing them with byte permutes; each of
+// its 4 output rows leaves as one 16-byte run.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) transpose_weight_128x128_kernel(const uint4* __restrict__ q, int64_t NB,
-                                                                       int64_t KB, int64_t ldq_v,
+__global__ void __launch_bounds__(256) transpose_weight_128x128_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                                       int64_t NB, int64_t KB,
                                                                        const float* __restrict__ sw,
                                                                        uint4* __restrict__ qt, int64_t ldqt_v,
-                                                                       float* __restrict__ swt) {
+                                                                       float* __restrict__ swt, unsigned* status,
+                                                                       uint64_t timeout_ns) {
   pdl_wait();
-  __shared__ __align__(16) uint8_t blk[128 * 128];
+  __shared__ __align__(128) uint8_t blk[128 * 128];
+  __shared__ __align__(8) uint64_t bar_storage;
+  const uint32_t bar = smem_u32(&bar_storage);
   const int cg = threadIdx.x & 31;  // input columns 4 cg .. 4 cg + 3 = output rows
   const int rg = threadIdx.x >> 5;  // input rows 16 rg .. 16 rg + 15 = output columns
   const int64_t nb = blockIdx.x;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmQ);
+  }
+  __syncthreads();
+  uint32_t parity = 0;
   for (int64_t kb = blockIdx.y; kb < KB; kb += gridDim.y) {
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int idx = threadIdx.x + 256 * i;  // 1024 chunks of 16 bytes
-      v[i] = ld_nc_v4(q + (nb * 128 + (idx >> 3)) * ldq_v + kb * 8 + (idx & 7));
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(bar, 128 * 128);
+      tma_load_2d(smem_u32(blk), &tmQ, bar, static_cast<int32_t>(kb * 128), static_cast<int32_t>(nb * 128));
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int idx = threadIdx.x + 256 * i;
-      *reinterpret_cast<uint4*>(blk + (idx >> 3) * 128 + (idx & 7) * 16) = v[i];
+    const bool landed = mbar_wait(bar, parity, nullptr, timeout_ns);
+    if (!__syncthreads_and(landed)) {
+      // let the copy in flight land before shared memory goes away
+      if (threadIdx.x == 0) {
+        record_status(status, kStatusTimeout);
+        (void)mbar_wait(bar, parity, nullptr, timeout_ns);
+      }
+      return;
     }
-    __syncthreads();
+    parity ^= 1u;
     uint32_t o[4][4];  // o[c][w]: output row 4 cg + c, bytes of input rows 16 rg + 4 w .. + 3
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -270,11 +282,13 @@ cudaError_t launch_requant_act_1x128_t(const DeviceInfo& dev, const void* qa, in
 cudaError_t launch_transpose_weight_128x128(const DeviceInfo& dev, const void* q, int64_t N, int64_t K, int64_t ldq,
                                             const float* sw, void* qt, int64_t ldqt, float* swt,
                                             cudaStream_t stream) {
-  (void)dev;
   const int64_t NB = N / 128, KB = K / 128;
+  CUtensorMap tmQ;
+  if (!make_tmap_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, K, N, ldq, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(NB), static_cast<unsigned>(KB < kMaxGridY ? KB : kMaxGridY));
-  (void)launch_pdl(transpose_weight_128x128_kernel, grid, 256, 0, stream, static_cast<const uint4*>(q), NB, KB, ldq / 16, sw,
-                                                            static_cast<uint4*>(qt), ldqt / 16, swt);
+  (void)launch_pdl(transpose_weight_128x128_kernel, grid, 256, 0, stream, tmQ, NB, KB, sw, static_cast<uint4*>(qt),
+                   ldqt / 16, swt, dev.status, wait_timeout_ns());
   return cudaGetLastError();
 }
 
