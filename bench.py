@@ -1109,6 +1109,10 @@ def run_ours(args):
             sms = stamped[0][k]
             a_st = units / (sms * 1e-3) / (1e12 if bound == "tensor" else 1e9)
             kern[k].update({"us_in_step": sms * 1e3, "achieved_in_step": a_st, "frac_in_step": a_st / peak})
+        # the kernel's figure: its share of the step by device timestamps when
+        # that pass ran (graph-timed steps), else its event interval
+        kern[k]["us"] = kern[k].get("us_in_step", kern[k]["us_events"])
+        kern[k]["frac"] = kern[k].get("frac_in_step", kern[k]["frac_events"])
     dominant = max(per_kernel, key=per_kernel.get)
     d = kern[dominant]
     roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved_events"], "peak": d["peak"],
@@ -1154,7 +1158,7 @@ def run_ours(args):
             "roofline": roofline,
             "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for k, v in kern.items()},
-            "tflops_gemm_only": flops / (per_kernel[step.kernels[-1]] * 1e-3) / 1e12,
+            "tflops_gemm_only": flops / (kern[step.kernels[-1]]["us"] * 1e-6) / 1e12,
             "timing": {"timed_region": f"{args.steps} steps, {launch_mode}, CUDA events on the launching stream",
                        "kernels_events": f"us_events: a second pass of {args.steps} stream-launched steps with a "
                                          "CUDA event after each kernel; a kernel's time includes the full launch "
@@ -1163,6 +1167,9 @@ def run_ours(args):
                                           "a device-timestamp kernel after each kernel; a kernel's time runs from "
                                           "the previous kernel's end to its own, as in the timed graph, plus "
                                           "about one short launch for the timestamp",
+                       "kernels_us_frac": "us and frac: us_in_step and frac_in_step when the timestamp pass ran, "
+                                          "else us_events and frac_events; the roofline object keeps the event "
+                                          "figure as frac and adds frac_in_step",
                        "attribution_pass_ms_per_step": attribution_ms,
                        "stamp_pass_ms_per_step": stamped[1] if stamped is not None else None,
                        "stamp_pass_clocks": ({k: stamped[2].get(k) for k in ("sm_mhz", "reasons", "samples")}
