@@ -620,11 +620,23 @@ def stamp_attribution(step, stream, steps, device):
         raise RuntimeError(f"device status word {status} after the timestamp pass")
     t = st.t.cpu().tolist()
     del g
-    per_kernel = {k: 0.0 for k in step.kernels}
+    per_kernel, step_ms = stamp_intervals(t, step.kernels, steps)
+    return per_kernel, step_ms, sampler.summary(t0, t1)
+
+
+def stamp_intervals(t, kernels, steps):
+    """Per-kernel ms per step from the timestamps (ns) of a stamped run: t[0]
+    before the first kernel, then one after each kernel of each step in
+    order.  Kernel i of a step gets the interval ending at its own stamp.
+    Returns ({kernel: ms per step}, ms per step from the first to the last
+    stamp)."""
+    nk = len(kernels)
+    if len(t) != steps * nk + 1:
+        raise ValueError("one timestamp before the steps and one after each kernel")
+    per_kernel = {k: 0.0 for k in kernels}
     for i in range(steps * nk):
-        per_kernel[step.kernels[i % nk]] += (t[i + 1] - t[i]) * 1e-6
-    clocks = sampler.summary(t0, t1)
-    return {k: v / steps for k, v in per_kernel.items()}, (t[-1] - t[0]) * 1e-6 / steps, clocks
+        per_kernel[kernels[i % nk]] += (t[i + 1] - t[i]) * 1e-6
+    return {k: v / steps for k, v in per_kernel.items()}, (t[-1] - t[0]) * 1e-6 / steps
 
 
 def time_e2e(name, inp, step, stream, steps, warmup, device, fb):

@@ -43,3 +43,38 @@ def test_gemm_launch_count_mirrors_the_launcher():
     assert bench.gemm_kernel_launches(128, 256, 256, 148) == 1
     assert bench.gemm_kernel_launches(2048, 2560, 6144, 148) == 2
     assert bench.gemm_kernel_launches(64, 7168, 18432, 148) == 2
+
+
+def test_stamp_intervals_split_the_steps():
+    """Each kernel's share is the interval ending at its own timestamp,
+    averaged over the steps; the shares add up to the stamped step."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    kernels = ["weight_quant", "act_quant", "gemm"]
+    # two steps: 64, 17, 425 us and 66, 15, 427 us after a first stamp at 1000 ns
+    t = [1000]
+    for us in (64, 17, 425, 66, 15, 427):
+        t.append(t[-1] + us * 1000)
+    per, step_ms = bench.stamp_intervals(t, kernels, 2)
+    assert per == {"weight_quant": 0.065, "act_quant": 0.016, "gemm": 0.426}
+    assert abs(step_ms - sum(per.values())) < 1e-12
+    import pytest
+
+    with pytest.raises(ValueError):
+        bench.stamp_intervals(t[:-1], kernels, 2)
+
+
+def test_clock_summary_from_samples():
+    """Median SM clock, minimum and the throttle reasons seen between the
+    region's host times, from (time, MHz, reason bits) samples."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.samples = [(0.0, 1000.0, 0), (1.0, 2032.0, 0), (2.0, 2010.0, 0x4), (3.0, 1990.0, 0), (9.0, 500.0, 0x40)]
+    cs.max_mhz, cs.nv, cs.error = 2032.0, object(), None
+    out = cs.summary(0.5, 3.5, ms=10.0)
+    assert out["sm_mhz"] == 2010.0 and out["sm_mhz_min"] == 1990.0 and out["samples"] == 3
+    assert out["reasons"] == ["sw_power_cap"] and out["region_ms_x_median_mhz"] == 20100.0
+    assert cs.summary(4.0, 5.0)["reasons"] == ["unsampled"]
