@@ -837,7 +837,7 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # Per-row measurements: every kernel of the scope table on its own, at full
 # size, against its roofline, with the CPU oracle timed on a bounded sample
-# in the same unit.  One JSON line per row (not the default line).
+# in the same unit.  One JSON line per row, apart from the step's benchmark line.
 # ---------------------------------------------------------------------------
 _FLUSH = None
 
