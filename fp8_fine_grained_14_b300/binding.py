@@ -530,13 +530,18 @@ class HostPipeline:
     three phases use three CUDA streams and `depth` sets of device buffers, so
     the copies of one batch overlap the kernels and copies of its neighbours.
     All arithmetic runs in the library's kernels; this class only owns
-    buffers, streams and events.
+    buffers, streams, events and graphs.
 
     prequantised_w: a (qw, sw) pair already on the device (decode-style
     serving, where the weights stay resident); then only X moves per batch.
+
+    use_graph: the kernels of each buffer set are captured once, at
+    construction, into a CUDA graph that every submit replays (one launch
+    instead of three C-ABI calls, which matters when the kernels are short).
+    If the capture fails the calls are made directly, still on the GPU.
     """
 
-    def __init__(self, M, N, K, device="cuda", depth=2, prequantised_w=None):
+    def __init__(self, M, N, K, device="cuda", depth=2, prequantised_w=None, use_graph=True):
         dev = torch.device(device)
         self.M, self.N, self.K, self.depth = M, N, K, depth
         self.h2d = torch.cuda.Stream(dev)
@@ -546,19 +551,52 @@ class HostPipeline:
         self.slots = []
         for _ in range(depth):
             slot = {
-                "x": torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                "x": torch.zeros((M, K), dtype=torch.bfloat16, device=dev),
                 "qa": torch.empty((M, K), dtype=torch.uint8, device=dev),
                 "sa": torch.empty((K // 128, ld_sa_for(M)), dtype=torch.float32, device=dev),
                 "y": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
                 "loaded": torch.cuda.Event(), "computed": torch.cuda.Event(), "stored": torch.cuda.Event(),
-                "used": False,
+                "used": False, "graph": None,
             }
             if prequantised_w is None:
-                slot["w"] = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+                slot["w"] = torch.zeros((N, K), dtype=torch.bfloat16, device=dev)
                 slot["qw"] = torch.empty((N, K), dtype=torch.uint8, device=dev)
                 slot["sw"] = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
             self.slots.append(slot)
         self.next = 0
+        if use_graph:
+            self._capture_all(dev)
+
+    def _compute(self, slot):
+        """The slot's kernels, in order, on the compute stream."""
+        fp8_quant_act_1x128(slot["x"], qa=slot["qa"], sa=slot["sa"], stream=self.compute)
+        if self.fixed_w is None:
+            fp8_quant_weight_128x128(slot["w"], qw=slot["qw"], sw=slot["sw"], stream=self.compute)
+            qw, sw = slot["qw"], slot["sw"]
+        else:
+            qw, sw = self.fixed_w
+        fp8_blockscaled_gemm(slot["qa"], slot["sa"], qw, sw, y=slot["y"], stream=self.compute)
+
+    def _capture_all(self, dev):
+        # one direct run per slot first: the library's per-device set-up
+        # (synchronous runtime calls) must not happen inside a capture
+        for slot in self.slots:
+            self._compute(slot)
+        torch.cuda.synchronize(dev)
+        try:
+            for slot in self.slots:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.compute, capture_error_mode="relaxed"):
+                    self._compute(slot)
+                slot["graph"] = g
+        except Exception:  # e.g. a driver without the needed capture support
+            torch.cuda.synchronize(dev)
+            for slot in self.slots:
+                slot["graph"] = None
+
+    @property
+    def graphed(self):
+        return all(slot["graph"] is not None for slot in self.slots)
 
     def submit(self, x_host, w_host, y_host):
         """Queue one batch; returns the event that completes when y_host holds Y."""
@@ -574,13 +612,11 @@ class HostPipeline:
         self.compute.wait_event(slot["loaded"])
         if slot["used"]:
             self.compute.wait_event(slot["stored"])  # previous Y of the slot copied out
-        fp8_quant_act_1x128(slot["x"], qa=slot["qa"], sa=slot["sa"], stream=self.compute)
-        if self.fixed_w is None:
-            fp8_quant_weight_128x128(slot["w"], qw=slot["qw"], sw=slot["sw"], stream=self.compute)
-            qw, sw = slot["qw"], slot["sw"]
+        if slot["graph"] is not None:
+            with torch.cuda.stream(self.compute):
+                slot["graph"].replay()
         else:
-            qw, sw = self.fixed_w
-        fp8_blockscaled_gemm(slot["qa"], slot["sa"], qw, sw, y=slot["y"], stream=self.compute)
+            self._compute(slot)
         slot["computed"].record(self.compute)
         self.d2h.wait_event(slot["computed"])
         with torch.cuda.stream(self.d2h):
