@@ -921,7 +921,7 @@ constexpr int kStagesPair = 4;
 constexpr bool kUsePairs = true;
 constexpr int kStages256 = 4;    // BN = 256 on one CTA: 48 KB stages
 constexpr int kStages128 = 6;    // BN = 128 on one CTA: 32 KB stages
-constexpr int kStages128HalfA = 8;  // BN = 128, 64-row A tiles (M <= 64): 24 KB stages
+constexpr int kStages128HalfA = 6;  // BN = 128, 64-row A tiles (M <= 64): 24 KB stages (6 measured 1% faster than 8, 4 slower)
 // Row-scaled B stages its column scales in shared memory: one stage fewer.
 constexpr int kStagesPairRS = 5;
 constexpr int kStages256RS = 3;
