@@ -180,9 +180,7 @@ __global__ void selftest_wait_kernel(unsigned* status, uint64_t timeout_ns) {
 __global__ void stream_timestamp_kernel(uint64_t* dst, int release) {
   if (release) pdl_launch_dependents();
   pdl_wait();
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  *dst = t;
+  *dst = globaltimer_ns();
 }
 
 }  // namespace
