@@ -681,7 +681,10 @@ def time_e2e(name, inp, step, stream, steps, warmup, device, fb):
     sync()
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
-    return wall / steps * 1e3, wall, h2d, d2h
+    mode = ("stream-ordered copies and calls" if name == "grouped" else
+            "HostPipeline, kernels replayed from CUDA graphs" if pipe.graphed else
+            f"HostPipeline, direct calls ({pipe.capture_error})")
+    return wall / steps * 1e3, wall, h2d, d2h, mode
 
 
 # ---------------------------------------------------------------------------
@@ -1150,10 +1153,10 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
-        ms, wall, h2d, d2h = time_e2e(name, inp, step, stream, e2e_steps, 2, device, fb)
+        ms, wall, h2d, d2h, mode = time_e2e(name, inp, step, stream, e2e_steps, 2, device, fb)
         ms = max_over_ranks(dist, ms, device)
         e2e = {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": e2e_steps}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": e2e_steps, "path": mode}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -564,6 +564,7 @@ class HostPipeline:
                 slot["sw"] = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
             self.slots.append(slot)
         self.next = 0
+        self.capture_error = None  # why the kernels are called directly, if capture failed
         if use_graph:
             self._capture_all(dev)
 
@@ -589,8 +590,9 @@ class HostPipeline:
                 with torch.cuda.graph(g, stream=self.compute, capture_error_mode="relaxed"):
                     self._compute(slot)
                 slot["graph"] = g
-        except Exception:  # e.g. a driver without the needed capture support
+        except Exception as e:  # e.g. a driver without the needed capture support
             torch.cuda.synchronize(dev)
+            self.capture_error = f"{type(e).__name__}: {e}"
             for slot in self.slots:
                 slot["graph"] = None
 
