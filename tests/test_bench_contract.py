@@ -23,7 +23,14 @@ def test_reference_arm_json_line():
     assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert d["unit"] == "TFLOP/s" and d["data"] == "synthetic"
-    assert "workload" in d["config"]
+    # the CUDA arm builds its config from the same workload, step and world size
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert d["config"] == bench.arm_config("up", 4096, 18432, 7168, 1, ["weight_quant", "act_quant", "gemm"], 1)
+    assert bench.step_kernels("up") == ["weight_quant", "act_quant", "gemm"]
+    assert bench.step_kernels("decode") == ["act_quant", "gemm"]
+    assert bench.step_kernels("grouped") == ["weight_quant", "act_quant", "grouped_gemm"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
