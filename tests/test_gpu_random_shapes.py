@@ -1,0 +1,169 @@
+"""Parity over seeded random shapes: the forward path (1x128 activation
+quantisation, 128x128 weight quantisation, the block-scaled GEMM with BF16,
+FP32 and residual outputs) and the grouped GEMM, on shapes drawn at random
+rather than picked by hand, so that tile-shape choices (64-row, 128-wide,
+256-wide and CTA-pair tiles; split and unsplit K tails; ragged M and empty
+groups) meet sizes nobody chose for them.
+
+Scale groups as in "The Definitive Information To Deepseek", "Figure 7 (a)";
+the GEMM as in its paragraphs 1 and 4 (FP8 chunk products promoted with the
+two scales, BF16 or FP32 out).  Codes and scales are compared bit for bit, Y
+within |y_gpu - y_ref| <= 1e-2 |y_ref| + 1e-3 rms(y_ref); the BF16 and
+residual outputs are also checked bit for bit against the FP32 output of the
+same call (one rounding, and one FP32 addition of R before it).
+
+Shape recipe (numpy default_rng, fixed seeds): M log-uniform within each
+case's range, N and K multiples of 128, M*N*K capped so that the oracle
+finishes each case in seconds; the "pair" cases take N a multiple of 256 and
+enough 128-row tiles to fill the 148 SMs' worth of 256-wide tiles.  Values:
+workloads.dense_inputs with a drawn weight scale and, in half the cases, a
+few activation channels scaled up (down-projection-like outliers)."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_fine_grained_14_b300 as fb
+import oracle
+from fp8_fine_grained_14_b300 import workloads
+from helpers import assert_codes_equal, assert_gemm_close, assert_scales_equal, f32, u8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+MAX_MACS = 6e9
+
+# (kind, M range, N range in 128-blocks, K range in 128-blocks)
+_KINDS = {
+    "skinny": ((1, 64), (1, 64), (1, 24)),
+    "narrow": ((65, 1500), (1, 24), (1, 12)),
+    "pair": ((1200, 2700), (8, 20), (1, 8)),
+}
+
+
+def _draw_dense(kind, seed):
+    rng = np.random.default_rng(seed)
+    (m0, m1), (n0, n1), (k0, k1) = _KINDS[kind]
+    while True:
+        M = int(np.exp(rng.uniform(np.log(m0), np.log(m1 + 1))))
+        M = min(max(M, m0), m1)
+        nb = int(rng.integers(n0, n1 + 1))
+        if kind == "pair":
+            nb += nb % 2  # N a multiple of 256
+        N, K = 128 * nb, 128 * int(rng.integers(k0, k1 + 1))
+        if kind == "pair" and -(-M // 128) * (N // 256) < 148:
+            continue
+        if M * N * K <= MAX_MACS:
+            break
+    w_std = float(10.0 ** rng.uniform(-3, 0))
+    outliers = bool(rng.integers(0, 2))
+    return M, N, K, w_std, outliers
+
+
+_DENSE = [(kind, 1000 + 17 * i) for i, kind in
+          enumerate(["skinny"] * 5 + ["narrow"] * 5 + ["pair"] * 4)]
+
+
+@pytest.mark.parametrize("kind,seed", _DENSE)
+def test_random_dense(kind, seed):
+    M, N, K, w_std, outliers = _draw_dense(kind, seed)
+    x, w = workloads.dense_inputs(M, N, K, seed=seed, w_std=w_std,
+                                  outlier_frac=0.01 if outliers else 0.0, outlier_scale=100.0)
+    g = torch.Generator().manual_seed(seed + 1)
+    r = (torch.randn((M, N), generator=g) * 0.5).to(torch.bfloat16)
+    xd, wd, rd = x.to(DEV), w.to(DEV), r.to(DEV)
+    y, (qa, sa, qw, sw) = fb.linear_forward(xd, wd)
+    y32 = fb.fp8_blockscaled_gemm(qa, sa, qw, sw, out_dtype=torch.float32)
+    yr = fb.fp8_blockscaled_gemm_residual(qa, sa, qw, sw, rd)
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    what = f"{kind} M={M} N={N} K={K}"
+
+    y_ref, (qa_r, sa_r, qw_r, sw_r) = oracle.linear_forward(f32(x), f32(w))
+    assert_codes_equal(u8(qa), qa_r, f"qa {what}")
+    assert_scales_equal(f32(sa)[:, :M], sa_r, f"sa {what}")
+    assert_codes_equal(u8(qw), qw_r, f"qw {what}")
+    assert_scales_equal(f32(sw), sw_r, f"sw {what}")
+    assert_gemm_close(f32(y), y_ref, what=f"bf16 {what}")
+    assert_gemm_close(f32(y32), y_ref, what=f"f32 {what}")
+    yr_ref = oracle.blockscaled_gemm_residual(qa_r, sa_r, qw_r, sw_r, f32(r))
+    assert_gemm_close(f32(yr), yr_ref, what=f"residual {what}")
+    # one epilogue, one FP32 accumulator: BF16 = RNE(FP32), residual = RNE(FP32 + R)
+    assert np.array_equal(oracle.bf16_round(f32(y32)).view(np.uint32), f32(y).view(np.uint32))
+    host_sum = oracle.bf16_round(np.float32(f32(y32)) + np.float32(f32(r)))
+    assert np.array_equal(host_sum.view(np.uint32), f32(yr).view(np.uint32))
+
+
+def test_random_dense_cover_both_tails():
+    """The drawn shapes include K tails that are split and ones that are not
+    (the workspace query says which, without launching anything)."""
+    split = [fb.fp8_blockscaled_gemm_workspace_bytes(*_draw_dense(kind, seed)[:3]) > 0 for kind, seed in _DENSE]
+    assert any(split) and not all(split), split
+
+
+def _draw_counts(rng):
+    G = int(rng.integers(1, 11))
+    counts = []
+    for _ in range(G):
+        u = rng.uniform()
+        if u < 0.15:
+            counts.append(0)
+        elif u < 0.5:
+            counts.append(int(rng.integers(1, 131)))
+        elif u < 0.8:
+            counts.append(max(0, 256 * int(rng.integers(1, 4)) + int(rng.integers(-2, 3))))
+        else:
+            counts.append(int(rng.integers(1, 701)))
+    return counts
+
+
+@pytest.mark.parametrize("seed", [2000, 2001, 2002, 2003, 2004, 2005])
+def test_random_grouped(seed):
+    rng = np.random.default_rng(seed)
+    counts = _draw_counts(rng)
+    G = len(counts)
+    N = 128 * int(rng.choice([1, 2, 3, 4, 8]))
+    K = 128 * int(rng.integers(1, 7))
+    offsets = workloads.grouped_offsets(counts)
+    m_total = int(offsets[-1])
+    x, _ = workloads.dense_inputs(max(m_total, 1), 128, K, seed=seed)
+    x = x[:m_total]
+    _, w = workloads.dense_inputs(1, G * N, K, seed=seed + 1)
+    w = w.reshape(G, N, K)
+    qa, sa = fb.fp8_quant_act_1x128(x.to(DEV))
+    qw, sw = fb.fp8_quant_weight_128x128(w.to(DEV))
+    y = fb.fp8_blockscaled_grouped_gemm(offsets.to(DEV), m_total, qa, sa, qw, sw)
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    what = f"counts={counts} N={N} K={K}"
+    qa_r, sa_r = oracle.quant_act_1x128(f32(x))
+    qw_r, sw_r = oracle.quant_weight_128x128(f32(w).reshape(G * N, K))
+    assert_codes_equal(u8(qa), qa_r, f"qa {what}")
+    assert_scales_equal(f32(sa)[:, :m_total], sa_r, f"sa {what}")
+    assert_codes_equal(u8(qw).reshape(G * N, K), qw_r, f"qw {what}")
+    assert_scales_equal(f32(sw).reshape(G * N // 128, K // 128), sw_r, f"sw {what}")
+    y_ref = oracle.blockscaled_grouped_gemm(offsets.numpy(), qa_r, sa_r, qw_r.reshape(G, N, K),
+                                            sw_r.reshape(G, N // 128, K // 128))
+    assert_gemm_close(f32(y), y_ref, what=f"grouped {what}")
+
+
+@pytest.mark.parametrize("seed", [3000, 3001, 3002, 3003, 3004, 3005])
+def test_random_quant(seed):
+    """Both quantisers on drawn shapes, with row magnitudes spread over 2^-60
+    .. 2^60 (every row's scale far from the others')."""
+    rng = np.random.default_rng(seed)
+    M = int(rng.integers(1, 3001))
+    K = 128 * int(rng.integers(1, 33))
+    N = 128 * int(rng.integers(1, 33))
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= (2.0 ** rng.integers(-60, 61, size=(M, 1))).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 10.0 ** rng.uniform(-3, 1)).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    wb = torch.from_numpy(w).to(torch.bfloat16)
+    qa, sa = fb.fp8_quant_act_1x128(xb.to(DEV))
+    qw, sw = fb.fp8_quant_weight_128x128(wb.to(DEV))
+    torch.cuda.synchronize()
+    qa_r, sa_r = oracle.quant_act_1x128(f32(xb))
+    qw_r, sw_r = oracle.quant_weight_128x128(f32(wb))
+    assert_codes_equal(u8(qa), qa_r, f"qa M={M} K={K}")
+    assert_scales_equal(f32(sa)[:, :M], sa_r, f"sa M={M} K={K}")
+    assert_codes_equal(u8(qw), qw_r, f"qw N={N} K={K}")
+    assert_scales_equal(f32(sw), sw_r, f"sw N={N} K={K}")
