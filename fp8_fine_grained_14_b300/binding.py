@@ -409,11 +409,18 @@ def fp8_blockscaled_gemm_rowscaled(qa, sa, qb, sb, y=None, stream=None, out_dtyp
     return y
 
 
+def _codes_out(M, K, device):
+    """A [M, K] code buffer whose row stride is K rounded up to 16 bytes (the
+    C ABI's rule for FP8 row strides), so that K % 16 == 8 works too."""
+    return torch.empty((M, (K + 15) // 16 * 16), dtype=torch.uint8, device=device)[:, :K]
+
+
 def fp8_quant_per_token(x, q=None, s=None, stream=None):
-    """x bf16 [M, K] -> (q uint8 [M, K], s float32 [M]): one scale per row."""
+    """x bf16 [M, K] -> (q uint8 [M, K], s float32 [M]): one scale per row.
+    A q given by the caller needs a row stride that is a multiple of 16."""
     _require(x, torch.bfloat16, "x", 2)
     M, K = x.shape
-    q = q if q is not None else torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    q = q if q is not None else _codes_out(M, K, x.device)
     s = s if s is not None else torch.empty((M,), dtype=torch.float32, device=x.device)
     _require_min(q, torch.uint8, "q", M, K)
     _require_count(s, "s", M)
@@ -423,10 +430,11 @@ def fp8_quant_per_token(x, q=None, s=None, stream=None):
 
 
 def fp8_quant_per_channel(x, q=None, s=None, stream=None):
-    """x bf16 [M, K] -> (q uint8 [M, K], s float32 [K]): one scale per column."""
+    """x bf16 [M, K] -> (q uint8 [M, K], s float32 [K]): one scale per column.
+    A q given by the caller needs a row stride that is a multiple of 16."""
     _require(x, torch.bfloat16, "x", 2)
     M, K = x.shape
-    q = q if q is not None else torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    q = q if q is not None else _codes_out(M, K, x.device)
     s = s if s is not None else torch.empty((K,), dtype=torch.float32, device=x.device)
     _require_min(q, torch.uint8, "q", M, K)
     _require_count(s, "s", K)

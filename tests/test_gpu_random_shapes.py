@@ -1,9 +1,11 @@
 """Parity over seeded random shapes: the forward path (1x128 activation
 quantisation, 128x128 weight quantisation, the block-scaled GEMM with BF16,
-FP32 and residual outputs) and the grouped GEMM, on shapes drawn at random
-rather than picked by hand, so that tile-shape choices (64-row, 128-wide,
-256-wide and CTA-pair tiles; split and unsplit K tails; ragged M and empty
-groups) meet sizes nobody chose for them.
+FP32 and residual outputs), the grouped GEMM, both backward GEMMs (X in BF16
+and from its FP8 cache), the GEMM on packed weight tiles, and the per-token
+and per-channel quantisers, on shapes drawn at random rather than picked by
+hand, so that tile-shape choices (64-row, 128-wide, 256-wide and CTA-pair
+tiles; split and unsplit K tails; ragged M and empty groups) meet sizes
+nobody chose for them.
 
 Scale groups as in "The Definitive Information To Deepseek", "Figure 7 (a)";
 the GEMM as in its paragraphs 1 and 4 (FP8 chunk products promoted with the
@@ -167,3 +169,75 @@ def test_random_quant(seed):
     assert_scales_equal(f32(sa)[:, :M], sa_r, f"sa M={M} K={K}")
     assert_codes_equal(u8(qw), qw_r, f"qw N={N} K={K}")
     assert_scales_equal(f32(sw), sw_r, f"sw N={N} K={K}")
+
+
+@pytest.mark.parametrize("seed", [4000, 4001, 4002, 4003, 4004])
+def test_random_backward(seed):
+    """Both backward GEMMs on drawn shapes (tokens M a multiple of 128, the
+    weight-gradient contraction), with X in BF16 and from its FP8 forward
+    cache ("The Definitive Information To Deepseek", paragraphs 2 and 3)."""
+    rng = np.random.default_rng(seed)
+    while True:
+        M = 128 * int(rng.integers(1, 17))
+        N = 128 * int(rng.integers(1, 25))
+        K = 128 * int(rng.integers(1, 17))
+        if M * N * K <= 3e9:
+            break
+    x, w, dy = workloads.backward_inputs(M, N, K, seed=seed, w_std=float(10.0 ** rng.uniform(-3, 0)))
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    dx, dw = fb.linear_backward(xd, wd, dyd)
+    qa, sa = fb.fp8_quant_act_1x128(xd)
+    dx_c, dw_c = fb.linear_backward(None, wd, dyd, x_cache=(qa, sa))
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    what = f"M={M} N={N} K={K}"
+    dx_ref, dw_ref = oracle.linear_backward(f32(x), f32(w), f32(dy))
+    assert_gemm_close(f32(dx), dx_ref, what=f"dX {what}")
+    assert_gemm_close(f32(dw), dw_ref, what=f"dW {what}")
+    qa_r, sa_r = oracle.quant_act_1x128(f32(x))
+    _, dw_c_ref = oracle.linear_backward_cached(qa_r, sa_r, f32(w), f32(dy))
+    assert torch.equal(dx_c, dx)  # dX does not depend on where X comes from
+    assert_gemm_close(f32(dw_c), dw_c_ref, what=f"dW from the FP8 cache {what}")
+
+
+@pytest.mark.parametrize("seed", [5000, 5001, 5002, 5003])
+def test_random_packed(seed):
+    """The GEMM on packed weight tiles, on drawn skinny shapes (the
+    weight-streaming case it serves): within the GEMM tolerance of the
+    oracle."""
+    rng = np.random.default_rng(seed)
+    M = int(rng.integers(1, 129))
+    N = 128 * int(rng.integers(1, 49))
+    K = 128 * int(rng.integers(1, 33))
+    x, w = workloads.dense_inputs(M, N, K, seed=seed)
+    qa, sa = fb.fp8_quant_act_1x128(x.to(DEV))
+    qw, sw = fb.fp8_quant_weight_128x128(w.to(DEV))
+    wp = fb.fp8_pack_weight_128x128(qw)
+    y = fb.fp8_blockscaled_gemm_packed(qa, sa, wp, sw)
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    y_ref, _ = oracle.linear_forward(f32(x), f32(w))
+    assert_gemm_close(f32(y), y_ref, what=f"packed M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("seed", [6000, 6001, 6002, 6003, 6004])
+def test_random_per_token_and_per_channel(seed):
+    """The per-token and per-channel quantisers on drawn shapes (K a multiple
+    of 8), rows and columns of widely spread magnitudes, bit for bit."""
+    rng = np.random.default_rng(seed)
+    M = int(rng.integers(1, 5001))
+    K = 8 * int(rng.integers(1, 513))
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= (2.0 ** rng.integers(-40, 41, size=(M, 1))).astype(np.float32)
+    x *= (2.0 ** rng.integers(-20, 21, size=(1, K))).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    xd = xb.to(DEV)
+    qt, st = fb.fp8_quant_per_token(xd)
+    qc, sc = fb.fp8_quant_per_channel(xd)
+    torch.cuda.synchronize()
+    qt_r, st_r = oracle.quant_per_token(f32(xb))
+    qc_r, sc_r = oracle.quant_per_channel(f32(xb))
+    assert_codes_equal(u8(qt), qt_r, f"per-token codes M={M} K={K}")
+    assert_scales_equal(f32(st), st_r, f"per-token scales M={M} K={K}")
+    assert_codes_equal(u8(qc), qc_r, f"per-channel codes M={M} K={K}")
+    assert_scales_equal(f32(sc), sc_r, f"per-channel scales M={M} K={K}")
