@@ -241,3 +241,73 @@ def test_random_per_token_and_per_channel(seed):
     assert_scales_equal(f32(st), st_r, f"per-token scales M={M} K={K}")
     assert_codes_equal(u8(qc), qc_r, f"per-channel codes M={M} K={K}")
     assert_scales_equal(f32(sc), sc_r, f"per-channel scales M={M} K={K}")
+
+
+@pytest.mark.parametrize("seed", [7000, 7001, 7002, 7003])
+def test_random_transposed_operands(seed):
+    """The weight-gradient operands on drawn shapes: 1x128 tiles of X^T from
+    BF16 X and from X's FP8 cache (dequantised to BF16, then requantised),
+    the 128x128 code and scale transpose of W, and the block dequant of W,
+    all bit for bit."""
+    rng = np.random.default_rng(seed)
+    M = 128 * int(rng.integers(1, 25))
+    K = 128 * int(rng.integers(1, 41))
+    N = 128 * int(rng.integers(1, 25))
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x *= (2.0 ** rng.integers(-30, 31, size=(1, K))).astype(np.float32)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    _, w = workloads.dense_inputs(1, N, K, seed=seed, w_std=float(10.0 ** rng.uniform(-3, 1)))
+    xd = xb.to(DEV)
+    qxt, sxt = fb.fp8_quant_act_1x128_t(xd)
+    qa, sa = fb.fp8_quant_act_1x128(xd)
+    qrt, srt = fb.fp8_requant_act_1x128_t(qa, sa)
+    qw, sw = fb.fp8_quant_weight_128x128(w.to(DEV))
+    qwt, swt = fb.fp8_transpose_weight_128x128(qw, sw)
+    wd = fb.fp8_dequant_weight_128x128(qw, sw)
+    torch.cuda.synchronize()
+    assert fb.fp8bs_last_device_error() == 0
+    what = f"M={M} N={N} K={K}"
+    q_ref, s_ref = oracle.quant_act_1x128_t(f32(xb))
+    assert_codes_equal(u8(qxt), q_ref, f"codes of x^T {what}")
+    assert_scales_equal(f32(sxt)[:, :K], s_ref, f"scales of x^T {what}")
+    qa_r, sa_r = oracle.quant_act_1x128(f32(xb))
+    qr_ref, sr_ref = oracle.requant_act_1x128_t(qa_r, sa_r)
+    assert_codes_equal(u8(qrt), qr_ref, f"requantised codes {what}")
+    assert_scales_equal(f32(srt)[:, :K], sr_ref, f"requantised scales {what}")
+    qw_r, sw_r = oracle.quant_weight_128x128(f32(w))
+    qwt_r, swt_r = oracle.transpose_weight_128x128(qw_r, sw_r)
+    assert_codes_equal(u8(qwt), qwt_r, f"codes of W^T {what}")
+    assert_scales_equal(f32(swt), swt_r, f"scales of W^T {what}")
+    wd_ref = oracle.dequant_weight_128x128_bf16(qw_r, sw_r)
+    assert np.array_equal(f32(wd).view(np.uint32), wd_ref.view(np.uint32)), f"dequant {what}"
+
+
+@pytest.mark.parametrize("seed", [8000, 8001, 8002])
+def test_random_e5m6_and_swiglu(seed):
+    """E5M6 round trips of drawn lengths (a multiple of 8), and the SwiGLU +
+    1x128 quantiser on drawn shapes: codes bit for bit given the kernel's own
+    BF16 product, which stays within a few ulps of the float64 product."""
+    rng = np.random.default_rng(seed)
+    n = 8 * int(rng.integers(1, 200001))
+    v = (rng.standard_normal(n) * 2.0 ** rng.integers(-20, 21, size=n)).astype(np.float32)
+    vb = torch.from_numpy(v).to(torch.bfloat16)
+    codes = fb.e5m6_encode(vb.to(DEV))
+    back = fb.e5m6_decode(codes)
+    M = int(rng.integers(1, 3001))
+    F = 128 * int(rng.integers(1, 25))
+    gu = torch.from_numpy((rng.standard_normal((M, 2 * F)) * 3.0).astype(np.float32)).to(torch.bfloat16)
+    qa, sa, h = fb.fp8_swiglu_quant_act_1x128(gu.to(DEV), return_h=True)
+    torch.cuda.synchronize()
+    vf = f32(vb)
+    want = oracle.e5m6_encode_rne_satfinite(vf)
+    assert np.array_equal(codes.cpu().numpy().view(np.uint16), want), f"e5m6 codes n={n}"
+    assert np.array_equal(f32(back).astype(np.float64), oracle.e5m6_decode(want)), f"e5m6 decode n={n}"
+    hg = f32(h)
+    q_ref, s_ref = oracle.quant_act_1x128(hg)
+    assert_codes_equal(u8(qa), q_ref, f"swiglu codes M={M} F={F}")
+    assert_scales_equal(f32(sa)[:, :M], s_ref, f"swiglu scales M={M} F={F}")
+    guf = f32(gu)
+    h64 = oracle.silu_mul(guf[:, :F], guf[:, F:])
+    a = np.abs(h64)
+    ulp_bf16 = 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-38))) - 7)
+    assert np.all(np.abs(hg - h64) <= 0.5 * ulp_bf16 + a * 2.0 ** -20), f"swiglu product M={M} F={F}"
