@@ -85,3 +85,24 @@ def test_clock_summary_from_samples():
     assert out["sm_mhz"] == 2010.0 and out["sm_mhz_min"] == 1990.0 and out["samples"] == 3
     assert out["reasons"] == ["sw_power_cap"] and out["region_ms_x_median_mhz"] == 20100.0
     assert cs.summary(4.0, 5.0)["reasons"] == ["unsampled"]
+
+
+def test_reference_arm_under_two_ranks():
+    """Launched as the multi-GPU run is (torchrun, two ranks): rank 0 alone
+    times the oracle and prints the one JSON line, with n_gpus = 2; the other
+    rank exits 0 without work."""
+    import socket
+
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+                          "--master-addr", "127.0.0.1", "--master-port", str(port),
+                          os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["config"]["parallelism"] == "replicas x2"
